@@ -1,0 +1,514 @@
+// Host side of the CONF-KV C ABI (include/confkv.h): context lifetime,
+// argument validation, launch sequencing of the per-step kernels, counters
+// and inspection.  No host/device synchronisation happens on the step path.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdint>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/confkv.h"
+#include "confkv_internal.cuh"
+
+using confkv::AttnParams;
+using confkv::Cache;
+using confkv::DevStats;
+using confkv::StepParams;
+
+namespace {
+
+constexpr int kSmCount = 152;
+constexpr int kProfKernels = 4;
+const char* const kProfNames[kProfKernels] = {"confidence", "select", "compact", "attention"};
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&prev);
+    if (dev >= 0 && dev != prev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+struct confkv_ctx {
+  int L = 0, B = 0, Hq = 0, Hkv = 0, d = 0, g = 0, V = 0;
+  int N_low = 0, N_high = 0, P = 0, W = 0, Ncap = 0, cap8 = 0, slots = 0;
+  int max_context = 0, device = 0, splits = 1;
+  float tau = 0.f, beta = 0.f, omb = 0.f, pyramid_min = 1.f;
+  int64_t t = 0, steps = 0;
+  bool prefilled = false;
+  Cache cache{};
+  float* conf = nullptr;
+  int32_t* hi = nullptr;
+  int32_t* btab = nullptr;
+  float* part_ml = nullptr;
+  float* part_acc = nullptr;
+  unsigned int* ticket = nullptr;
+  float* seed_out = nullptr;
+  std::vector<void*> allocs;
+  // staging of confkv_step_host
+  float* st_logits = nullptr;
+  uint16_t* st_q = nullptr;
+  uint16_t* st_k = nullptr;
+  uint16_t* st_v = nullptr;
+  float* st_out = nullptr;
+  int32_t* st_kp = nullptr;
+  int32_t* st_kc = nullptr;
+  float* st_conf = nullptr;
+  int32_t* st_bud = nullptr;
+  std::string msg = "ok";
+  // profiling
+  bool prof = false;
+  std::vector<cudaEvent_t> ev[kProfKernels];   // start/stop pairs
+  double prof_ms[kProfKernels] = {0, 0, 0, 0};
+  long long prof_n[kProfKernels] = {0, 0, 0, 0};
+};
+
+namespace {
+
+int fail(confkv_ctx* c, int code, const std::string& m) {
+  if (c) c->msg = m;
+  return code;
+}
+
+template <typename T>
+cudaError_t dalloc(confkv_ctx* c, T** p, size_t count) {
+  void* q = nullptr;
+  const cudaError_t e = cudaMalloc(&q, std::max<size_t>(count, 1) * sizeof(T));
+  if (e != cudaSuccess) return e;
+  c->allocs.push_back(q);
+  *p = static_cast<T*>(q);
+  return cudaMemset(q, 0, std::max<size_t>(count, 1) * sizeof(T));
+}
+
+void free_all(confkv_ctx* c) {
+  for (void* p : c->allocs) cudaFree(p);
+  c->allocs.clear();
+  for (int k = 0; k < kProfKernels; ++k) {
+    for (cudaEvent_t e : c->ev[k]) cudaEventDestroy(e);
+    c->ev[k].clear();
+  }
+}
+
+// CONF-KV-L: linear per-layer factor from 1 (layer 0) to pyramid_min (last
+// layer), rounded to nearest, never below the protected window.
+int layer_budget(int N, int l, int L, double pmin, int P) {
+  const double f = (L > 1) ? 1.0 - (1.0 - pmin) * static_cast<double>(l) / static_cast<double>(L - 1)
+                           : 1.0;
+  const int n = static_cast<int>(std::floor(static_cast<double>(N) * f + 0.5));
+  return std::max(P, n);
+}
+
+void prof_mark(confkv_ctx* c, int k, cudaStream_t s) {
+  if (!c->prof) return;
+  cudaEvent_t e;
+  if (cudaEventCreate(&e) != cudaSuccess) return;
+  cudaEventRecord(e, s);
+  c->ev[k].push_back(e);
+}
+
+void prof_collect(confkv_ctx* c) {
+  for (int k = 0; k < kProfKernels; ++k) {
+    std::vector<cudaEvent_t>& v = c->ev[k];
+    for (size_t i = 0; i + 1 < v.size(); i += 2) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, v[i], v[i + 1]) == cudaSuccess) {
+        c->prof_ms[k] += ms;
+        c->prof_n[k] += 1;
+      }
+    }
+    for (cudaEvent_t e : v) cudaEventDestroy(e);
+    v.clear();
+  }
+}
+
+int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s) {
+  AttnParams ap{};
+  ap.q = q;
+  ap.out = out;
+  ap.splits = c->splits;
+  ap.part_ml = c->part_ml;
+  ap.part_acc = c->part_acc;
+  ap.ticket = c->ticket;
+  ap.scale = 1.0f / std::sqrt(static_cast<float>(c->d));
+  const cudaError_t e = confkv::launch_attention(c->cache, ap, s);
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("attention launch: ") + cudaGetErrorString(e));
+  return CONFKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, int N_high,
+                  float tau, int P, int W, float ema_decay, const confkv_opts* opts,
+                  confkv_ctx** out) {
+  if (!out) return CONFKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  confkv_opts o{};
+  if (opts) o = *opts;
+  if (o.batch == 0) o.batch = 1;
+  const float pmin = (o.pyramid_min == 0.0f) ? 1.0f : o.pyramid_min;
+  if (layers < 1 || heads < 1 || kv_heads < 1 || heads % kv_heads != 0 ||
+      heads / kv_heads > confkv::kMaxGroup || (head_dim != 64 && head_dim != 128) || P < 1 ||
+      W < P || N_low < P || N_high < P || !(ema_decay >= 0.0f && ema_decay <= 1.0f) ||
+      !std::isfinite(tau) || o.batch < 1 || o.vocab < 2 || o.max_context < 0 ||
+      !(pmin > 0.0f && pmin <= 1.0f) || o.attn_splits < 0 || o.attn_splits > 64)
+    return CONFKV_ERR_INVALID_ARG;
+  int dev = o.device;
+  if (!opts || dev < 0) cudaGetDevice(&dev);
+  DeviceGuard guard(dev);
+  confkv_ctx* c = new confkv_ctx();
+  c->L = layers;
+  c->B = o.batch;
+  c->Hq = heads;
+  c->Hkv = kv_heads;
+  c->d = head_dim;
+  c->g = heads / kv_heads;
+  c->V = o.vocab;
+  c->N_low = N_low;
+  c->N_high = N_high;
+  c->P = P;
+  c->W = W;
+  c->tau = tau;
+  c->beta = ema_decay;
+  c->omb = 1.0f - ema_decay;
+  c->pyramid_min = pmin;
+  c->max_context = o.max_context;
+  c->device = dev;
+  c->Ncap = std::max(N_low, N_high);
+  c->cap8 = std::max(std::max(0, o.max_context - W), c->Ncap);
+  c->cap8 = (c->cap8 + 15) / 16 * 16;
+  c->slots = c->cap8 + W;
+
+  const size_t LB = static_cast<size_t>(c->L) * c->B;
+  const size_t U = LB * c->Hkv;
+  const int units = static_cast<int>(U);
+  if (o.attn_splits > 0) {
+    c->splits = o.attn_splits;
+  } else {
+    const int want = (4 * kSmCount + units - 1) / units;
+    const int tok_lim = std::max(1, (c->Ncap + 1 + 127) / 128);
+    c->splits = std::max(1, std::min(std::min(want, tok_lim), 16));
+  }
+
+  Cache& k = c->cache;
+  k.L = c->L; k.B = c->B; k.Hq = c->Hq; k.Hkv = c->Hkv; k.d = c->d; k.g = c->g;
+  k.W = c->W; k.P = c->P; k.cap8 = c->cap8; k.slots = c->slots; k.Ncap = c->Ncap;
+  cudaError_t e = cudaSuccess;
+  auto A = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+  A(dalloc(c, &k.k8, U * c->cap8 * c->d));
+  A(dalloc(c, &k.v8, U * c->cap8 * c->d));
+  A(dalloc(c, &k.ks, U * c->cap8));
+  A(dalloc(c, &k.vs, U * c->cap8));
+  A(dalloc(c, &k.k16, U * c->W * c->d));
+  A(dalloc(c, &k.v16, U * c->W * c->d));
+  A(dalloc(c, &k.pos8, LB * c->cap8));
+  A(dalloc(c, &k.pos16, LB * c->W));
+  A(dalloc(c, &k.ema8, LB * c->cap8));
+  A(dalloc(c, &k.ema16, LB * c->W));
+  A(dalloc(c, &k.mass, U * c->slots));
+  A(dalloc(c, &k.scores, LB * c->Hq * c->slots));
+  A(dalloc(c, &k.keys, LB * c->slots));
+  A(dalloc(c, &k.n8, LB));
+  A(dalloc(c, &k.n16, LB));
+  A(dalloc(c, &k.jobs8, LB * c->cap8));
+  A(dalloc(c, &k.jobs16, LB * c->W));
+  A(dalloc(c, &k.njobs, LB * 2));
+  A(dalloc(c, &k.stats, 1));
+  A(dalloc(c, &k.err, 1));
+  A(dalloc(c, &c->conf, c->B));
+  A(dalloc(c, &c->hi, c->B));
+  A(dalloc(c, &c->btab, static_cast<size_t>(c->L) * 2));
+  A(dalloc(c, &c->part_ml, LB * c->Hq * c->splits * 2));
+  A(dalloc(c, &c->part_acc, LB * c->Hq * c->splits * c->d));
+  A(dalloc(c, &c->ticket, U));
+  A(dalloc(c, &c->seed_out, LB * c->Hq * c->d));
+  if (e == cudaSuccess) {
+    std::vector<int32_t> bt(static_cast<size_t>(c->L) * 2);
+    for (int l = 0; l < c->L; ++l) {
+      bt[l * 2] = layer_budget(N_low, l, c->L, pmin, P);
+      bt[l * 2 + 1] = layer_budget(N_high, l, c->L, pmin, P);
+    }
+    e = cudaMemcpy(c->btab, bt.data(), bt.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    const bool oom = (e == cudaErrorMemoryAllocation);
+    cudaGetLastError();
+    free_all(c);
+    delete c;
+    return oom ? CONFKV_ERR_OOM : CONFKV_ERR_CUDA;
+  }
+  *out = c;
+  return CONFKV_OK;
+}
+
+int confkv_prefill(confkv_ctx* c, const uint16_t* k, const uint16_t* v, int T,
+                   const uint16_t* q_last, void* stream) {
+  if (!c) return CONFKV_ERR_INVALID_ARG;
+  if (c->steps > 0 || c->prefilled) return fail(c, CONFKV_ERR_STATE, "prefill must precede every step and happen once");
+  if (T < 0) return fail(c, CONFKV_ERR_INVALID_ARG, "T < 0");
+  if (T > c->max_context) return fail(c, CONFKV_ERR_CAPACITY, "T exceeds max_context");
+  if (T > 0 && (!k || !v)) return fail(c, CONFKV_ERR_INVALID_ARG, "null k or v");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 1u)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "misaligned k or v");
+  DeviceGuard guard(c->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  c->prefilled = true;
+  c->t = T;
+  if (T == 0) return CONFKV_OK;
+  cudaError_t e = confkv::launch_prefill_store(c->cache, reinterpret_cast<const __half*>(k),
+                                               reinterpret_cast<const __half*>(v), T, s);
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("prefill: ") + cudaGetErrorString(e));
+  if (q_last) return run_attention(c, reinterpret_cast<const __half*>(q_last), c->seed_out, s);
+  return CONFKV_OK;
+}
+
+int confkv_step(confkv_ctx* c, const float* logits, const uint16_t* q, const uint16_t* k_new,
+                const uint16_t* v_new, float* out, int32_t* kept_pos, int32_t* kept_count,
+                float* conf_out, int32_t* budget_out, void* stream) {
+  if (!c) return CONFKV_ERR_INVALID_ARG;
+  if (!logits || !q || !k_new || !v_new || !out)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "null logits, q, k_new, v_new or out");
+  if (c->t >= 0x7fffffffLL) return fail(c, CONFKV_ERR_STATE, "position overflow");
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(out) |
+       reinterpret_cast<uintptr_t>(q)) & 3u)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "misaligned logits, q or out");
+  DeviceGuard guard(c->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  prof_mark(c, 0, s);
+  e = confkv::launch_confidence(logits, c->B, c->V, c->tau, c->N_low, c->N_high, c->conf, c->hi,
+                                conf_out, budget_out, c->cache.err, c->cache.stats, s);
+  prof_mark(c, 0, s);
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("confidence: ") + cudaGetErrorString(e));
+  StepParams sp{};
+  sp.t = static_cast<int>(c->t);
+  sp.beta = c->beta;
+  sp.omb = c->omb;
+  sp.btab = c->btab;
+  sp.hi = c->hi;
+  sp.kept_pos = kept_pos;
+  sp.kept_count = kept_count;
+  prof_mark(c, 1, s);
+  e = confkv::launch_select(c->cache, sp, s);
+  prof_mark(c, 1, s);
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("select: ") + cudaGetErrorString(e));
+  prof_mark(c, 2, s);
+  e = confkv::launch_compact(c->cache, reinterpret_cast<const __half*>(k_new),
+                             reinterpret_cast<const __half*>(v_new), s);
+  prof_mark(c, 2, s);
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("compact: ") + cudaGetErrorString(e));
+  prof_mark(c, 3, s);
+  const int rc = run_attention(c, reinterpret_cast<const __half*>(q), out, s);
+  prof_mark(c, 3, s);
+  if (rc != CONFKV_OK) return rc;
+  c->t += 1;
+  c->steps += 1;
+  return CONFKV_OK;
+}
+
+int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
+                     const uint16_t* k_new, const uint16_t* v_new, float* out,
+                     int32_t* kept_pos, int32_t* kept_count, float* conf_out,
+                     int32_t* budget_out, void* stream) {
+  if (!c) return CONFKV_ERR_INVALID_ARG;
+  if (!logits || !q || !k_new || !v_new || !out)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "null logits, q, k_new, v_new or out");
+  DeviceGuard guard(c->device);
+  const size_t LB = static_cast<size_t>(c->L) * c->B;
+  const size_t nlog = static_cast<size_t>(c->B) * c->V, nq = LB * c->Hq * c->d,
+               nkv = LB * c->Hkv * c->d, nkp = LB * c->Ncap;
+  cudaError_t e = cudaSuccess;
+  auto A = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+  if (!c->st_logits) {
+    A(dalloc(c, &c->st_logits, nlog));
+    A(dalloc(c, &c->st_q, nq));
+    A(dalloc(c, &c->st_k, nkv));
+    A(dalloc(c, &c->st_v, nkv));
+    A(dalloc(c, &c->st_out, nq));
+    A(dalloc(c, &c->st_kp, nkp));
+    A(dalloc(c, &c->st_kc, LB));
+    A(dalloc(c, &c->st_conf, c->B));
+    A(dalloc(c, &c->st_bud, c->B));
+    if (e != cudaSuccess) return fail(c, e == cudaErrorMemoryAllocation ? CONFKV_ERR_OOM : CONFKV_ERR_CUDA, "staging allocation");
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  A(cudaMemcpyAsync(c->st_logits, logits, nlog * sizeof(float), cudaMemcpyHostToDevice, s));
+  A(cudaMemcpyAsync(c->st_q, q, nq * 2, cudaMemcpyHostToDevice, s));
+  A(cudaMemcpyAsync(c->st_k, k_new, nkv * 2, cudaMemcpyHostToDevice, s));
+  A(cudaMemcpyAsync(c->st_v, v_new, nkv * 2, cudaMemcpyHostToDevice, s));
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("H2D: ") + cudaGetErrorString(e));
+  const int rc = confkv_step(c, c->st_logits, c->st_q, c->st_k, c->st_v, c->st_out,
+                             kept_pos ? c->st_kp : nullptr, kept_count ? c->st_kc : nullptr,
+                             conf_out ? c->st_conf : nullptr, budget_out ? c->st_bud : nullptr,
+                             stream);
+  if (rc != CONFKV_OK) return rc;
+  A(cudaMemcpyAsync(out, c->st_out, nq * sizeof(float), cudaMemcpyDeviceToHost, s));
+  if (kept_pos) A(cudaMemcpyAsync(kept_pos, c->st_kp, nkp * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  if (kept_count) A(cudaMemcpyAsync(kept_count, c->st_kc, LB * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  if (conf_out) A(cudaMemcpyAsync(conf_out, c->st_conf, c->B * sizeof(float), cudaMemcpyDeviceToHost, s));
+  if (budget_out) A(cudaMemcpyAsync(budget_out, c->st_bud, c->B * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  A(cudaStreamSynchronize(s));
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("D2H: ") + cudaGetErrorString(e));
+  return CONFKV_OK;
+}
+
+int confkv_stats(confkv_ctx* c, confkv_stats_t* out) {
+  if (!c || !out) return CONFKV_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("sync: ") + cudaGetErrorString(e));
+  DevStats ds{};
+  int32_t err = 0;
+  const size_t LB = static_cast<size_t>(c->L) * c->B;
+  std::vector<int32_t> n8(LB), n16(LB);
+  e = cudaMemcpy(&ds, c->cache.stats, sizeof(ds), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&err, c->cache.err, sizeof(err), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(n8.data(), c->cache.n8, LB * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(n16.data(), c->cache.n16, LB * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(c->cache.err, 0, sizeof(int32_t));
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("stats: ") + cudaGetErrorString(e));
+  std::memset(out, 0, sizeof(*out));
+  out->steps = c->steps;
+  out->position = c->t;
+  out->error_flags = err;
+  out->tokens_evicted = static_cast<int64_t>(ds.evicted);
+  out->tokens_quantized = static_cast<int64_t>(ds.quantized);
+  out->tokens_moved = static_cast<int64_t>(ds.moved);
+  out->attn_kv_bytes = static_cast<int64_t>(ds.kv_bytes);
+  out->logits_bytes = static_cast<int64_t>(ds.logits_bytes);
+  out->budget_high_steps = static_cast<int64_t>(ds.hi_steps);
+  int64_t tok = 0;
+  double bytes = 0.0;
+  for (size_t i = 0; i < LB; ++i) {
+    tok += n8[i] + n16[i];
+    bytes += static_cast<double>(c->Hkv) * (n8[i] * (2.0 * c->d + 8.0) + n16[i] * 4.0 * c->d);
+  }
+  out->cache_tokens = tok;
+  out->cache_bytes = bytes;
+  if (err & CONFKV_FLAG_TIMEOUT) return fail(c, CONFKV_ERR_DEVICE, "a device-side wait gave up");
+  if (err & CONFKV_FLAG_NONFINITE) return fail(c, CONFKV_ERR_NONFINITE_LOGITS, "non-finite logits seen");
+  if (err & CONFKV_FLAG_CAPACITY) return fail(c, CONFKV_ERR_CAPACITY, "cache capacity exceeded");
+  return CONFKV_OK;
+}
+
+int confkv_read_cache(confkv_ctx* c, int l, int b, int cap, int* n8o, int* n16o, int32_t* pos,
+                      float* ema, int8_t* k8, int8_t* v8, float* ks, float* vs, uint16_t* k16,
+                      uint16_t* v16, float* mass) {
+  if (!c || l < 0 || l >= c->L || b < 0 || b >= c->B || cap < 0)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "bad (l, b) or cap");
+  DeviceGuard guard(c->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  const size_t lb = static_cast<size_t>(l) * c->B + b;
+  int n8 = 0, n16 = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&n8, c->cache.n8 + lb, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&n16, c->cache.n16 + lb, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, cudaGetErrorString(e));
+  if (n8o) *n8o = n8;
+  if (n16o) *n16o = n16;
+  const int r8 = std::min(n8, cap), r16 = std::max(0, std::min(n16, cap - r8));
+  const int d = c->d, H = c->Hkv;
+  auto cp = [&](void* dst, const void* src, size_t bytes) {
+    if (e == cudaSuccess && bytes) e = cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost);
+  };
+  if (pos) {
+    cp(pos, c->cache.pos8 + lb * c->cap8, r8 * 4);
+    cp(pos + r8, c->cache.pos16 + lb * c->W, r16 * 4);
+  }
+  if (ema) {
+    cp(ema, c->cache.ema8 + lb * c->cap8, r8 * 4);
+    cp(ema + r8, c->cache.ema16 + lb * c->W, r16 * 4);
+  }
+  std::vector<int8_t> t8(static_cast<size_t>(std::max(r8, 1)) * d);
+  std::vector<float> tf(std::max(r8, 1));
+  std::vector<uint16_t> t16(static_cast<size_t>(std::max(r16, 1)) * d);
+  for (int h = 0; h < H; ++h) {
+    const size_t u = lb * H + h;
+    for (int which = 0; which < 2; ++which) {
+      int8_t* dst8 = which ? v8 : k8;
+      if (dst8 && r8) {
+        cp(t8.data(), (which ? c->cache.v8 : c->cache.k8) + u * c->cap8 * d, static_cast<size_t>(r8) * d);
+        for (int i = 0; i < r8; ++i)
+          std::memcpy(dst8 + (static_cast<size_t>(i) * H + h) * d, t8.data() + static_cast<size_t>(i) * d, d);
+      }
+      float* dsts = which ? vs : ks;
+      if (dsts && r8) {
+        cp(tf.data(), (which ? c->cache.vs : c->cache.ks) + u * c->cap8, static_cast<size_t>(r8) * 4);
+        for (int i = 0; i < r8; ++i) dsts[static_cast<size_t>(i) * H + h] = tf[i];
+      }
+      uint16_t* dst16 = which ? v16 : k16;
+      if (dst16 && r16) {
+        cp(t16.data(), reinterpret_cast<const uint16_t*>(which ? c->cache.v16 : c->cache.k16) + u * c->W * d,
+           static_cast<size_t>(r16) * d * 2);
+        for (int i = 0; i < r16; ++i)
+          std::memcpy(dst16 + (static_cast<size_t>(i) * H + h) * d, t16.data() + static_cast<size_t>(i) * d, d * 2);
+      }
+    }
+  }
+  if (mass) {
+    std::vector<float> m(static_cast<size_t>(c->slots));
+    for (int i = 0; i < r8 + r16; ++i) mass[i] = 0.0f;
+    for (int h = 0; h < H; ++h) {
+      cp(m.data(), c->cache.mass + (lb * H + h) * c->slots, static_cast<size_t>(c->slots) * 4);
+      for (int i = 0; i < r8; ++i) mass[i] += m[i];
+      for (int i = 0; i < r16; ++i) mass[r8 + i] += m[c->cap8 + i];
+    }
+    for (int i = 0; i < r8 + r16; ++i) mass[i] /= static_cast<float>(c->Hq);
+  }
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, cudaGetErrorString(e));
+  return CONFKV_OK;
+}
+
+int confkv_profile_enable(confkv_ctx* c, int enable) {
+  if (!c) return CONFKV_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!enable && c->prof) {
+    cudaDeviceSynchronize();
+    prof_collect(c);
+  }
+  if (enable && !c->prof) {
+    for (int k = 0; k < kProfKernels; ++k) { c->prof_ms[k] = 0.0; c->prof_n[k] = 0; }
+  }
+  c->prof = enable != 0;
+  return CONFKV_OK;
+}
+
+int confkv_profile_read(confkv_ctx* c, confkv_profile_t* out) {
+  if (!c || !out) return CONFKV_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  cudaDeviceSynchronize();
+  prof_collect(c);
+  std::memset(out, 0, sizeof(*out));
+  out->n_kernels = kProfKernels;
+  for (int k = 0; k < kProfKernels; ++k) {
+    out->launches[k] = static_cast<int32_t>(c->prof_n[k]);
+    out->total_ms[k] = c->prof_ms[k];
+    out->names[k] = kProfNames[k];
+  }
+  return CONFKV_OK;
+}
+
+const char* confkv_last_error(const confkv_ctx* c) { return c ? c->msg.c_str() : "null context"; }
+
+void confkv_free(confkv_ctx* c) {
+  if (!c) return;
+  DeviceGuard guard(c->device);
+  cudaDeviceSynchronize();
+  free_all(c);
+  delete c;
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// Internal device-side layout of the CONF-KV cache and launch wrappers.
+//
+// HBM layout of one context (lb = l*B + b, h = KV head):
+//   INT8 region   k8, v8  int8  [L*B][Hkv][cap8][d]    (slots 0..n8-1 live)
+//                 ks, vs  fp32  [L*B][Hkv][cap8]       one absmax scale per row
+//   FP16 region   k16,v16 fp16  [L*B][Hkv][W][d]       (slots 0..n16-1 live)
+//   metadata      pos8, ema8 [L*B][cap8]; pos16, ema16 [L*B][W]
+//   mass          fp32 [L*B][Hkv][slots]   attention mass of the last
+//                 attention summed over the query heads of one KV head;
+//                 slot id = INT8 slot, or cap8 + FP16 slot; slots = cap8 + W
+//   scores        fp32 [L*B][Hq][slots]    raw scores of the last attention
+// Both regions are dense (contiguous compaction): live slots are always
+// [0, n8) and [0, n16), so the attention streams them without any indirection.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace confkv {
+
+constexpr int kMaxGroup = 16;   // query heads per KV head supported
+
+struct DevStats {
+  unsigned long long evicted;
+  unsigned long long quantized;
+  unsigned long long moved;
+  unsigned long long kv_bytes;
+  unsigned long long logits_bytes;
+  unsigned long long hi_steps;
+};
+
+struct Cache {
+  int L, B, Hq, Hkv, d, g, W, P, cap8, slots, Ncap;
+  int8_t* k8;
+  int8_t* v8;
+  float* ks;
+  float* vs;
+  __half* k16;
+  __half* v16;
+  int32_t* pos8;
+  int32_t* pos16;
+  float* ema8;
+  float* ema16;
+  float* mass;
+  float* scores;
+  float* keys;      // [L*B][slots] ranking keys of the current step
+  int32_t* n8;
+  int32_t* n16;
+  int2* jobs8;      // [L*B][cap8]  (dst INT8 slot, src INT8 slot)
+  int2* jobs16;     // [L*B][W]     (dst FP16 slot, src FP16 slot or -1 = new token)
+  int32_t* njobs;   // [L*B][2]     INT8 moves, FP16 writes
+  DevStats* stats;
+  int32_t* err;
+};
+
+struct StepParams {
+  int t;                 // position of the new token
+  float beta, omb;       // EMA decay and 1 - decay (fp32)
+  const int32_t* btab;   // [L][2] per-layer budget for (N_low, N_high)
+  const int32_t* hi;     // [B] 1 if the sequence chose N_high
+  int32_t* kept_pos;     // [L*B][Ncap] or null
+  int32_t* kept_count;   // [L*B] or null
+};
+
+struct AttnParams {
+  const __half* q;       // [L*B][Hq][d]
+  float* out;            // [L*B][Hq][d]
+  int splits;
+  float* part_ml;        // [L*B*Hq][splits][2]
+  float* part_acc;       // [L*B*Hq][splits][d]
+  unsigned int* ticket;  // [L*B*Hkv]
+  float scale;           // 1/sqrt(d)
+};
+
+// ---- launch wrappers (each file owns its kernels) ----
+cudaError_t launch_confidence(const float* logits, int B, int V, float tau, int N_low,
+                              int N_high, float* conf, int32_t* hi, float* conf_out,
+                              int32_t* budget_out, int32_t* err, DevStats* st,
+                              cudaStream_t s);
+cudaError_t launch_select(const Cache& c, const StepParams& sp, cudaStream_t s);
+cudaError_t launch_compact(const Cache& c, const __half* k_new, const __half* v_new,
+                           cudaStream_t s);
+cudaError_t launch_prefill_store(const Cache& c, const __half* k, const __half* v, int T,
+                                 cudaStream_t s);
+cudaError_t launch_attention(const Cache& c, const AttnParams& ap, cudaStream_t s);
+
+}  // namespace confkv

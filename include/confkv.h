@@ -1,0 +1,207 @@
+/*
+ * confkv.h -- C ABI of the CONF-KV decode-step library for GB300 (sm_103a).
+ *
+ * Method: "CONF-KV: Confidence-Aware KV Cache Eviction with Mixed-Precision
+ * Storage for Long-Horizon LLM" (gist.science summaries of paper 2605.24786,
+ * "Technische Samenvatting" / "Riepilogo Tecnico" / "기술 요약").  Section
+ * names below are those of the Dutch page.
+ *
+ * One context manages the KV cache of every (layer, sequence) of a batch.
+ * Each decode step:
+ *   1. reduces each sequence's logits to a confidence
+ *        c = 0.4 (1 - H^) + 0.3 sigma(m) + 0.3 p(1)        [Vertrouwensschatting]
+ *   2. picks the budget N_high if c >= tau, else N_low   [Adaptieve Budgetselectie]
+ *      (optionally scaled per layer, CONF-KV-L)           [Pyramidale Budgetten]
+ *   3. updates each cached token's EMA attention mass, ranks tokens by
+ *      EMA mass + recency, keeps the best N, never evicting the newest P
+ *                                                         [Tokenrangschikking]
+ *   4. compacts the survivors contiguously and stores tokens older than the
+ *      newest W as INT8 (absmax, per token and KV head) [Mixed-Precision Opslag,
+ *                                                          Implementatie]
+ *   5. runs block-wise online-softmax decode attention with the INT8
+ *      dequantisation fused into the block reads           [Implementatie]
+ *
+ * Conventions for every call:
+ *   - fp16 tensors are IEEE binary16 bit patterns (uint16_t); fp32 is float.
+ *   - Tensor arguments of confkv_prefill / confkv_step are DEVICE pointers on
+ *     the context's GPU, contiguous, row-major in the stated layout, owned by
+ *     the caller, and only touched by work enqueued on `stream` during the
+ *     call.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   - The context owns all cache memory; it is single-threaded: calls on one
+ *     context must not run concurrently from several host threads.
+ *   - Calls return CONFKV_OK (0) or a negative CONFKV_ERR_* code.  Argument
+ *     errors are detected on the host before any work is enqueued; the
+ *     message is available from confkv_last_error().  Errors the GPU detects
+ *     (non-finite logits, a wait that timed out) are latched in device memory
+ *     and returned by the next confkv_stats() call.  No exception crosses the
+ *     ABI; no call traps the GPU.
+ *   - confkv_step never synchronises the host with the GPU and allocates
+ *     nothing, so a sequence of steps can be captured in a CUDA graph once
+ *     the context exists.
+ */
+#ifndef CONFKV_H_
+#define CONFKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CONFKV_OK 0
+#define CONFKV_ERR_INVALID_ARG (-1)   /* bad argument; nothing enqueued */
+#define CONFKV_ERR_CUDA (-2)          /* a CUDA runtime call failed */
+#define CONFKV_ERR_OOM (-3)           /* device allocation failed */
+#define CONFKV_ERR_CAPACITY (-4)      /* prefill longer than max_context */
+#define CONFKV_ERR_NONFINITE_LOGITS (-5) /* a NaN/+inf (or no finite) logit was seen */
+#define CONFKV_ERR_STATE (-6)         /* call out of order (e.g. prefill after steps) */
+#define CONFKV_ERR_DEVICE (-7)        /* a device-side wait gave up */
+
+/* device-side error flags (bit mask, confkv_stats_t.error_flags) */
+#define CONFKV_FLAG_NONFINITE 1
+#define CONFKV_FLAG_CAPACITY 2
+#define CONFKV_FLAG_TIMEOUT 4
+
+typedef struct confkv_ctx confkv_ctx;
+
+/* Optional settings of confkv_create (all fields may be zero = default). */
+typedef struct confkv_opts {
+  int batch;         /* B sequences decoded together (default 1) */
+  int vocab;         /* V, logits per sequence (required, >= 2) */
+  int max_context;   /* longest prefill T accepted by confkv_prefill (default 0) */
+  float pyramid_min; /* CONF-KV-L: budget factor of the last layer; the factor
+                        falls linearly from 1 at layer 0 (0 or 1 = uniform) */
+  int device;        /* CUDA device ordinal; negative = the current device
+                        (a NULL opts also means the current device) */
+  int attn_splits;   /* split-K factor of the attention (0 = automatic) */
+} confkv_opts;
+
+/* Counters read back by confkv_stats (cumulative since create unless noted). */
+typedef struct confkv_stats_t {
+  int64_t steps;            /* decode steps run */
+  int64_t position;         /* position of the next token */
+  int32_t error_flags;      /* CONFKV_FLAG_* bits latched since the last call */
+  int32_t reserved;
+  int64_t tokens_evicted;   /* over all (layer, sequence) */
+  int64_t tokens_quantized; /* FP16 -> INT8 conversions (prefill included) */
+  int64_t tokens_moved;     /* compaction moves */
+  int64_t cache_tokens;     /* current sum over (layer, sequence) of cached tokens */
+  int64_t attn_kv_bytes;    /* algorithmic KV + scale bytes read by attention */
+  int64_t logits_bytes;     /* logits bytes read by the confidence reduction */
+  int64_t budget_high_steps;/* (sequence, step) pairs that chose N_high */
+  double cache_bytes;       /* current bytes of cached K/V + scales */
+} confkv_stats_t;
+
+/* Per-kernel device time, accumulated while profiling is enabled. */
+typedef struct confkv_profile_t {
+  int32_t n_kernels;        /* entries used below */
+  int32_t launches[8];
+  double total_ms[8];
+  const char* names[8];     /* static strings */
+} confkv_profile_t;
+
+/*
+ * confkv_create -- allocate the cache manager of L layers x B sequences.
+ *   layers (L >= 1), heads (Hq query heads), kv_heads (Hkv; Hq % Hkv == 0,
+ *   Hq / Hkv <= 16), head_dim (d = 64 or 128).
+ *   N_low: budget chosen when c < tau; N_high: budget when c >= tau
+ *     [Adaptieve Budgetselectie]; both >= P.
+ *   tau: confidence threshold.
+ *   P: protected window, the newest P tokens are never evicted (P >= 1)
+ *     [Tokenrangschikking].
+ *   W: the newest W tokens stay FP16, older kept tokens are INT8 (W >= P)
+ *     [Mixed-Precision Opslag].
+ *   ema_decay: beta of ema <- beta*ema + (1-beta)*mass, in [0, 1].
+ *   opts: see confkv_opts (vocab is required).
+ *   *out receives the context.  Returns CONFKV_ERR_INVALID_ARG or
+ *   CONFKV_ERR_OOM on failure (then *out is NULL).
+ */
+int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low,
+                  int N_high, float tau, int P, int W, float ema_decay,
+                  const confkv_opts* opts, confkv_ctx** out);
+
+/*
+ * confkv_prefill -- store a prompt of T tokens (positions 0..T-1) in every
+ * (layer, sequence) cache.  No token is evicted; tokens whose age T-1-pos is
+ * >= W are stored as INT8.  Optional q_last seeds the attention mass that the
+ * first decode step folds into the EMA (the EMA itself stays 0).
+ *   k, v:   fp16 [L][B][Hkv][T][d] (device)
+ *   q_last: fp16 [L][B][Hq][d] (device) or NULL
+ * Must precede the first confkv_step; T <= max_context (else
+ * CONFKV_ERR_CAPACITY).  T == 0 is a no-op.
+ */
+int confkv_prefill(confkv_ctx* ctx, const uint16_t* k, const uint16_t* v, int T,
+                   const uint16_t* q_last, void* stream);
+
+/*
+ * confkv_step -- one decode step of every (layer, sequence): confidence,
+ * budget, EMA + ranking, eviction, compaction + INT8 aging, attention.
+ *   logits:  fp32 [B][V]          this step's next-token logits
+ *   q:       fp16 [L][B][Hq][d]   queries of the new token
+ *   k_new:   fp16 [L][B][Hkv][d]  key of the new token (appended, FP16)
+ *   v_new:   fp16 [L][B][Hkv][d]
+ *   out:     fp32 [L][B][Hq][d]   attention output over the kept cache
+ *   kept_pos:   int32 [L][B][N_max], N_max = max(N_low, N_high): positions of
+ *               the kept tokens, in cache slot order (INT8 region first);
+ *               entries past kept_count are left untouched.  May be NULL.
+ *   kept_count: int32 [L][B] tokens kept.  May be NULL.
+ *   conf_out:   fp32 [B] confidence c (NULL allowed)
+ *   budget_out: int32 [B] budget N of the sequence before the per-layer
+ *               pyramid factor (NULL allowed)
+ * Non-finite logits latch CONFKV_FLAG_NONFINITE and the step proceeds with
+ * c = 0 (budget N_low).
+ */
+int confkv_step(confkv_ctx* ctx, const float* logits, const uint16_t* q,
+                const uint16_t* k_new, const uint16_t* v_new, float* out,
+                int32_t* kept_pos, int32_t* kept_count, float* conf_out,
+                int32_t* budget_out, void* stream);
+
+/*
+ * confkv_step_host -- confkv_step with HOST buffers of the same layouts.
+ * Copies the inputs to context-owned device staging buffers, runs the step
+ * and copies the outputs back, all on `stream`, then waits for the stream.
+ * Pinned host memory makes the copies asynchronous DMA; pageable memory works
+ * but is slower.  NULL outputs are skipped.
+ */
+int confkv_step_host(confkv_ctx* ctx, const float* logits, const uint16_t* q,
+                     const uint16_t* k_new, const uint16_t* v_new, float* out,
+                     int32_t* kept_pos, int32_t* kept_count, float* conf_out,
+                     int32_t* budget_out, void* stream);
+
+/*
+ * confkv_stats -- synchronise the context's device and read the counters.
+ * Returns the first latched device error (CONFKV_ERR_NONFINITE_LOGITS or
+ * CONFKV_ERR_DEVICE) and clears the flags, else CONFKV_OK.
+ */
+int confkv_stats(confkv_ctx* ctx, confkv_stats_t* out);
+
+/*
+ * confkv_read_cache -- copy the cache of one (layer l, sequence b) to host
+ * memory for inspection (synchronises).  Rows are in slot order: INT8 slots
+ * first (n8 of them), then FP16 slots (n16).  Any pointer may be NULL.
+ *   pos [n], ema [n]  (int32, fp32)
+ *   k8, v8 [n8][Hkv][d] int8;  ks, vs [n8][Hkv] fp32 scales
+ *   k16, v16 [n16][Hkv][d] fp16 bits
+ *   mass [n] fp32: the attention mass of the last attention (mean over the
+ *   query heads), which the next step folds into the EMA
+ * *n8 and *n16 receive the region sizes; `cap` bounds n8 + n16 rows written.
+ */
+int confkv_read_cache(confkv_ctx* ctx, int l, int b, int cap, int* n8, int* n16,
+                      int32_t* pos, float* ema, int8_t* k8, int8_t* v8, float* ks,
+                      float* vs, uint16_t* k16, uint16_t* v16, float* mass);
+
+/* Enable (1) / disable (0) per-kernel CUDA-event timing, and read it. */
+int confkv_profile_enable(confkv_ctx* ctx, int enable);
+int confkv_profile_read(confkv_ctx* ctx, confkv_profile_t* out);
+
+/* Message of the last error of this context (never NULL). */
+const char* confkv_last_error(const confkv_ctx* ctx);
+
+/* Release the context and all its device memory (NULL is a no-op). */
+void confkv_free(confkv_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONFKV_H_ */

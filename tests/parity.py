@@ -1,0 +1,179 @@
+"""GPU-vs-oracle comparison driver shared by the parity tests.
+
+Both sides run free from the same seeded inputs; the oracle never receives a
+value computed on the GPU.  Per step and per (layer, sequence):
+  * confidence c within 1e-5 absolute; budget decisions identical, except where
+    |c_oracle - tau| < 1e-5 (counted as a budget divergence);
+  * kept-position sets identical, except where every differing token's oracle
+    ranking key lies within 1e-6 relative of the oracle's cut (counted);
+  * attention outputs within 1e-3 max-abs while the kept sets agree;
+  * INT8 codes, scales and FP16 rows bit-exact (by position) on checked steps.
+A (layer, sequence) that diverged legitimately is no longer compared (its
+future inputs to attention differ); its GPU-only invariants still are.
+"""
+import numpy as np
+import torch
+
+import oracle
+from synth import workloads as wl
+
+TOL_C = 1e-5
+TOL_OUT = 1e-3
+TOL_KEY_REL = 1e-6
+
+
+def to_dev(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+class Report:
+    def __init__(self):
+        self.compared = 0
+        self.kept_div = 0
+        self.budget_div = 0
+        self.code_checks = 0
+        self.max_out_err = 0.0
+        self.max_c_err = 0.0
+        self.total = 0
+
+    def __repr__(self):
+        return (f"compared={self.compared}/{self.total} kept_div={self.kept_div} "
+                f"budget_div={self.budget_div} code_checks={self.code_checks} "
+                f"max_out_err={self.max_out_err:.2e} max_c_err={self.max_c_err:.2e}")
+
+
+def _legit_kept_divergence(keys, kept_o, kept_g):
+    """Every differing token's oracle key within 1e-6 relative of the cut."""
+    key, pos, prot = keys["key"], keys["pos"], keys["prot"]
+    by_pos = {int(p): float(k) for p, k in zip(pos, key)}
+    cand_kept = [by_pos[p] for p in kept_o if p in by_pos and not prot[list(pos).index(p)]]
+    if not cand_kept:
+        return False
+    cut = min(cand_kept)
+    for p in kept_o ^ kept_g:
+        if p not in by_pos:
+            return False
+        if abs(by_pos[p] - cut) > TOL_KEY_REL * abs(cut):
+            return False
+    return True
+
+
+def compare_cache(kv, orc, l, b, rep):
+    g = kv.read_cache(l, b)
+    o = orc.tokens(l, b)
+    assert sorted(g["pos"].tolist()) == sorted(o["pos"].tolist())
+    oi = {int(p): i for i, p in enumerate(o["pos"])}
+    for i in range(g["n8"]):
+        j = oi[int(g["pos"][i])]
+        assert o["is8"][j], "GPU INT8 token is FP16 in the oracle"
+        assert np.array_equal(g["k8"][i], o["k8"][j]) and np.array_equal(g["v8"][i], o["v8"][j])
+        assert np.array_equal(g["ks"][i], o["ks"][j]) and np.array_equal(g["vs"][i], o["vs"][j])
+    for i in range(g["n16"]):
+        j = oi[int(g["pos"][g["n8"] + i])]
+        assert not o["is8"][j], "GPU FP16 token is INT8 in the oracle"
+        assert np.array_equal(g["k16"][i], o["k16"][j]) and np.array_equal(g["v16"][i], o["v16"][j])
+    rep.code_checks += 1
+
+
+def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, splits=0,
+        logits_override=None):
+    """Run workload `w` on the GPU and in the oracle; return a Report.
+
+    lbs: iterable of (l, b) the oracle simulates (default: all).
+    device_inputs: generate the GPU's inputs with the device generator (large
+      workloads); the oracle always uses the host generator.
+    logits_override: optional fn(s, logits) -> logits applied to both sides.
+    """
+    import confidence_gated_kv_logits_gb300 as pkg
+    dev = torch.device("cuda", 0)
+    steps = w.steps if steps is None else steps
+    kv = pkg.ConfKV.for_workload(w, device=0, attn_splits=splits)
+    orc = oracle.Oracle.for_workload(w)
+    all_lbs = [(l, b) for l in range(w.L) for b in range(w.B)]
+    lbs = all_lbs if lbs is None else list(lbs)
+    mask = np.zeros((w.L, w.B), np.uint8)
+    for l, b in lbs:
+        mask[l, b] = 1
+    orc.set_active(mask)
+    rep = Report()
+    # ---- prefill ----
+    if w.prefill:
+        if device_inputs:
+            from synth import device as sd
+            K, V = sd.prefill_kv(w)
+        else:
+            K = np.zeros((w.L, w.B, w.Hkv, w.prefill, w.d), np.float16)
+            V = np.zeros_like(K)
+        ql = wl.q_last(w)
+        for l, b in (lbs if device_inputs else all_lbs):
+            k, v = wl.prefill_kv_lb(w, l, b)
+            if not device_inputs:
+                K[l, b], V[l, b] = k, v
+            if mask[l, b]:
+                orc.prefill_lb(l, b, k, v, None if ql is None else ql[l, b])
+        if not device_inputs:
+            K, V = to_dev(K, dev), to_dev(V, dev)
+        kv.prefill(K, V, w.prefill, None if ql is None else to_dev(ql, dev))
+        del K, V
+    else:
+        orc.set_position(0)
+    out = torch.zeros(w.L, w.B, w.Hq, w.d, device=dev)
+    kp = torch.full((w.L, w.B, kv.Ncap), -1, dtype=torch.int32, device=dev)
+    kc = torch.zeros(w.L, w.B, dtype=torch.int32, device=dev)
+    cf = torch.zeros(w.B, device=dev)
+    bd = torch.zeros(w.B, dtype=torch.int32, device=dev)
+    diverged = set()
+    prev = {}
+    for s in range(steps):
+        lg, q, k, v = wl.step_inputs(w, s)
+        if logits_override is not None:
+            lg = logits_override(s, lg)
+        if device_inputs and logits_override is None:
+            from synth import device as sd
+            glg, gq, gk, gv = sd.step_inputs(w, s)
+        else:
+            glg, gq, gk, gv = (to_dev(x, dev) for x in (lg, q, k, v))
+        kv.step(glg, gq, gk, gv, out, kp, kc, cf, bd)
+        r = orc.step(lg, q, k, v, cap=kv.Ncap)
+        torch.cuda.synchronize()
+        g_out, g_kp, g_kc = out.cpu().numpy(), kp.cpu().numpy(), kc.cpu().numpy()
+        g_cf, g_bd = cf.cpu().numpy(), bd.cpu().numpy()
+        t = w.position(s)
+        for b in range(w.B):
+            rep.max_c_err = max(rep.max_c_err, abs(float(g_cf[b]) - r["conf"][b]))
+            assert abs(float(g_cf[b]) - r["conf"][b]) < TOL_C, (s, b, g_cf[b], r["conf"][b])
+            if g_bd[b] != r["budget"][b]:
+                assert abs(r["conf"][b] - w.tau) < TOL_C, (s, b)
+                rep.budget_div += 1
+                diverged |= {(l, b) for l in range(w.L)}
+        for l, b in lbs:
+            rep.total += 1
+            n = int(g_kc[l, b])
+            kept_g = set(g_kp[l, b, :n].tolist())
+            N = oracle.layer_budget(int(g_bd[b]), l, w.L, w.pyramid_min, w.P)
+            # GPU-only invariants
+            assert len(kept_g) == n <= max(N, 1)
+            assert set(range(max(0, t - w.P + 1), t + 1)) <= kept_g
+            if (l, b) in prev:
+                assert kept_g <= prev[(l, b)] | {t}
+            prev[(l, b)] = kept_g
+            if (l, b) in diverged:
+                continue
+            kept_o = set(r["kept_pos"][l, b, :r["kept_count"][l, b]].tolist())
+            if kept_g != kept_o:
+                assert _legit_kept_divergence(orc.last_keys(l, b), kept_o, kept_g), (
+                    s, l, b, sorted(kept_g ^ kept_o))
+                rep.kept_div += 1
+                diverged.add((l, b))
+                continue
+            err = float(np.max(np.abs(g_out[l, b] - r["out"][l, b])))
+            rep.max_out_err = max(rep.max_out_err, err)
+            assert err < TOL_OUT, (s, l, b, err)
+            rep.compared += 1
+            if check_codes_every and (s % check_codes_every == 0 or s == steps - 1):
+                compare_cache(kv, orc, l, b, rep)
+    st, rc = kv.stats(check=False)
+    kv.close()
+    rep.stats = st
+    rep.rc = rc
+    return rep

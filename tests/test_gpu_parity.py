@@ -1,0 +1,181 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Tolerances (from the method's contract): INT8 codes, budgets and kept sets
+bit-exact (kept-set near-ties within 1e-6 relative of the oracle's cut, and
+budget near-ties |c - tau| < 1e-5, are counted divergences); c within 1e-5
+absolute; attention outputs within 1e-3 max-abs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import gen, workloads as wl
+
+from . import parity
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+def small(**kw):
+    base = dict(name="small", L=2, B=3, Hq=8, Hkv=2, d=128, V=3000, prefill=0, steps=80,
+                N_high=48, N_low=72, P=8, W=24)
+    base.update(kw)
+    return wl.Workload(**base)
+
+
+# ---------------------------------------------------------------------------
+# input generator: device twin bit-identical to the host generator
+# ---------------------------------------------------------------------------
+
+def test_device_generator_bit_exact():
+    from synth import device as sd
+    shape = (3, 2, 5, 97, 64)
+    t = torch.empty(shape, dtype=torch.float16, device=DEV)
+    sd.fill_f16(t, 0, gen.KIND_KPRE, 0, heavy=True, inner=64, tlen=97, pos0=0)
+    ref = gen.gen_f16(0, gen.KIND_KPRE, 0, shape, inner=64, tlen=97, heavy=True).reshape(shape)
+    assert np.array_equal(t.cpu().numpy().view(np.uint16), ref.view(np.uint16))
+    lg = torch.empty(4, 50257, dtype=torch.float32, device=DEV)
+    sd.fill_logits(lg, 0, 7, 0.3)
+    ref = gen.gen_logits(0, 7, 4, 50257, 0.3)
+    assert np.array_equal(lg.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    w = wl.QWEN32B.with_(L=2, B=2, prefill=300)
+    dl, dq, dk, dv = sd.step_inputs(w, 5)
+    hl, hq, hk, hv = wl.step_inputs(w, 5)
+    for a, b in ((dl, hl), (dq, hq), (dk, hk), (dv, hv)):
+        assert np.array_equal(a.cpu().numpy(), b)
+
+
+# ---------------------------------------------------------------------------
+# confidence reduction and budget
+# ---------------------------------------------------------------------------
+
+def _conf_case(V, logits):
+    import confidence_gated_kv_logits_gb300 as pkg
+    B = logits.shape[0]
+    kv = pkg.ConfKV(1, 2, 1, 64, 8, 4, 0.5, 2, 4, 0.9, batch=B, vocab=V, device=0)
+    lg = torch.from_numpy(np.ascontiguousarray(logits)).to(DEV)
+    q = torch.zeros(1, B, 2, 64, dtype=torch.float16, device=DEV)
+    k = torch.zeros(1, B, 1, 64, dtype=torch.float16, device=DEV)
+    out = torch.zeros(1, B, 2, 64, device=DEV)
+    cf = torch.zeros(B, device=DEV)
+    bd = torch.zeros(B, dtype=torch.int32, device=DEV)
+    kv.step(lg, q, k, k, out, conf=cf, budget=bd)
+    st, rc = kv.stats(check=False)
+    kv.close()
+    return cf.cpu().numpy(), bd.cpu().numpy(), st, rc
+
+
+@pytest.mark.parametrize("V", [2, 7, 1000, 50257, 152064, 201088])
+def test_confidence_parity(V):
+    rng = np.random.default_rng(V)
+    B = 8
+    lg = np.empty((B, V), np.float32)
+    temps = [0.05, 0.1, 0.3, 0.3, 1.0, 3.0, 0.02, 10.0]
+    for b in range(B):
+        lg[b] = rng.standard_normal(V) / temps[b] + rng.uniform(-50, 50)
+    if V > 10:
+        lg[6, rng.choice(V, V // 3, replace=False)] = -np.inf      # masked tokens
+        lg[7, :] = 1.5                                              # uniform
+    c, bud, st, rc = _conf_case(V, lg)
+    assert rc == 0
+    for b in range(B):
+        co = oracle.confidence(lg[b])[0]
+        assert abs(c[b] - co) < 1e-5, (b, c[b], co)
+        if abs(co - 0.5) > 1e-5:
+            assert bud[b] == (4 if co >= 0.5 else 8)
+
+
+def test_confidence_nonfinite_is_flagged_not_fatal():
+    import confidence_gated_kv_logits_gb300 as pkg
+    lg = np.zeros((3, 100), np.float32)
+    lg[1, 5] = np.nan
+    lg[2, :] = -np.inf
+    c, bud, st, rc = _conf_case(100, lg)
+    assert rc == pkg.ERR_NONFINITE_LOGITS and st["error_flags"] & pkg.FLAG_NONFINITE
+    assert c[1] == 0 and c[2] == 0 and bud[1] == 8 and bud[2] == 8
+    assert abs(c[0] - oracle.confidence(lg[0])[0]) < 1e-5
+
+
+# ---------------------------------------------------------------------------
+# whole-step parity on small shapes (several tiles, ragged tails)
+# ---------------------------------------------------------------------------
+
+def _check(rep, min_frac=0.6):
+    print(rep)
+    assert rep.rc == 0, rep.rc
+    assert rep.compared >= min_frac * rep.total, rep
+    return rep
+
+
+def test_gqa_d128_decode_from_empty():
+    _check(parity.run(small(steps=120)))
+
+
+def test_gqa_d128_prefill_and_budget_drops():
+    w = small(prefill=150, L=2, B=3, Hq=40, Hkv=8, N_high=40, N_low=70, P=8, W=20, steps=60,
+              V=64)
+    rep = _check(parity.run(w))
+    assert rep.stats["tokens_evicted"] > 0 and rep.stats["tokens_moved"] > 0
+
+
+def test_mha_d64_gpt2_shape_1layer():
+    w = wl.GPT2_L1.with_(steps=900)
+    rep = _check(parity.run(w, check_codes_every=100))
+    assert rep.stats["tokens_evicted"] > 0
+
+
+def test_gqa8_d64_pyramid():
+    w = small(L=4, B=2, Hq=64, Hkv=8, d=64, pyramid_min=0.5, prefill=100, steps=50,
+              N_high=30, N_low=60, P=6, W=12, V=500)
+    _check(parity.run(w))
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_forced_split_counts(splits):
+    w = small(prefill=90, steps=40, V=64)
+    _check(parity.run(w, splits=splits))
+
+
+def test_sliding_window_special_case_is_exact():
+    # beta = 1 freezes the EMA: keys are pure recency, identical in both precisions
+    w = small(beta=1.0, prefill=60, steps=60, V=64)
+    rep = _check(parity.run(w), min_frac=1.0)
+    assert rep.kept_div == 0
+
+
+@pytest.mark.parametrize("P,W,N_high,N_low", [(1, 1, 1, 2), (5, 5, 5, 9), (8, 40, 8, 8),
+                                              (16, 16, 20, 17)])
+def test_edge_windows_and_budgets(P, W, N_high, N_low):
+    w = small(P=P, W=W, N_high=N_high, N_low=N_low, prefill=33, steps=45, V=64, L=1, B=2)
+    _check(parity.run(w))
+
+
+def test_short_context_noop():
+    w = small(N_high=500, N_low=500, W=500, P=8, prefill=70, steps=40)
+    rep = _check(parity.run(w), min_frac=1.0)
+    assert rep.stats["tokens_evicted"] == 0
+
+
+def test_prefill_shorter_than_window_and_empty_prefill():
+    _check(parity.run(small(prefill=10, W=24, steps=50)))
+    _check(parity.run(small(prefill=0, W=24, steps=30)))
+
+
+def test_needles_q_last_seed():
+    w = wl.QWEN14B.with_(L=2, B=1, prefill=2000, W=128, P=32, N_high=256, N_low=512,
+                         steps=12, needles=16, V=5000)
+    _check(parity.run(w))
+
+
+# ---------------------------------------------------------------------------
+# full-size shapes in the benchmark's launch configuration, sampled (l, b)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.slow
+def test_full_size_qwen32b_sampled():
+    w = wl.QWEN32B
+    lbs = [(0, 0), (31, 5), (63, 7)]
+    rep = _check(parity.run(w, steps=3, lbs=lbs, device_inputs=True, check_codes_every=2))
+    assert rep.stats["tokens_evicted"] > 0
