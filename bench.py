@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Decode throughput of the full CONF-KV step on GB300.
+
+Workload (default): Qwen-32B-shaped cache, 64 layers, 40 query / 8 KV heads,
+head_dim 128, vocab 152064, batch 8, 8192-token synthetic prefill, then
+decode steps with logits alternating 64-step temperature segments 0.3 / 3.0
+(tau 0.5, N_high 1024, N_low 2048, P 128, W 256, EMA decay 0.9).
+
+One "step" = one decode step of every layer and sequence: confidence,
+budget, EMA + ranking + eviction, compaction + INT8 aging, attention.
+Prefill is outside the timed region; the per-step inputs are resident in HBM
+before it starts.  Every step reads >1 GB of KV, far more than the 129 MB L2,
+so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun) every rank runs an independent replica (the path
+shards by sequence with no exchange): weak scaling, value = all ranks'
+tokens / the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s on 1 GB300 (full CONF-KV step); attention HBM GB/s vs peak"
+UNIT = "tokens/s"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_traffic.json")
+ATTN_SRC = os.path.join(ROOT, "confidence_gated_kv_logits_gb300", "csrc", "k_attention.cu")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=509)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="qwen32b-shaped-b8-p8192")
+    p.add_argument("--e2e-steps", type=int, default=128)
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--layers", type=int, default=0,
+                   help="profiling only: override the layer count (smaller capture)")
+    return p.parse_args()
+
+
+def get_workload(args):
+    from synth import workloads as wl
+    w = wl.ALL[args.workload]
+    if args.layers:
+        w = w.with_(L=args.layers, name=f"{w.name}-L{args.layers}")
+    return w
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)["hbm_gbs"], "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": w.name, "layers": w.L, "q_heads": w.Hq, "kv_heads": w.Hkv,
+           "head_dim": w.d, "vocab": w.V, "batch": w.B, "prefill": w.prefill,
+           "N_high": w.N_high, "N_low": w.N_low, "P": w.P, "W": w.W, "tau": w.tau,
+           "ema_decay": w.beta, "pyramid_min": w.pyramid_min,
+           "l2": "no flush: each step reads >1 GB of KV, inputs larger than L2"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.samples if t0 - 0.05 <= t <= t1 + 0.05] or \
+               [r for (_, r) in self.samples[-5:]]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, seconds, steps_cap=None):
+    """Time the oracle on a bounded sample of workload w; return tokens/s and notes.
+
+    Sample: one (layer, sequence) lane, prefilled like the GPU run, stepped from
+    decode step 1 on (step 0's prefill-sized eviction is run untimed); each
+    timed oracle step also computes all B confidences.  A full decode step
+    costs L*B lane-steps + B confidences, so
+        tokens/s = B / (L*B*t_lane + B*t_conf).
+    """
+    import numpy as np
+
+    import oracle
+    from synth import gen, workloads as wl
+    o = oracle.Oracle.for_workload(w)
+    mask = np.zeros((w.L, w.B), np.uint8)
+    lane = (w.L // 2, w.B // 2)
+    mask[lane] = 1
+    o.set_active(mask)
+    if w.prefill:
+        k, v = wl.prefill_kv_lb(w, *lane)
+        ql = wl.q_last_lb(w, *lane)
+        o.prefill_lb(lane[0], lane[1], k, v, ql)
+    else:
+        o.set_position(0)
+    t_lane = []
+    t_conf = []
+    s = 0
+    spent = 0.0
+    while True:
+        lg, q, kn, vn = wl.step_inputs_lane(w, s, *lane)
+        t0 = time.perf_counter()
+        o.step(lg, q, kn, vn)
+        t1 = time.perf_counter()
+        for b in range(w.B):
+            oracle.confidence(lg[b])
+        t2 = time.perf_counter()
+        if s > 0:
+            t_conf.append((t2 - t1) / w.B)
+            t_lane.append((t1 - t0) - (t2 - t1))
+            spent += t2 - t0
+        s += 1
+        if spent >= seconds or (steps_cap and s > steps_cap):
+            break
+    tl = statistics.mean(t_lane)
+    tc = statistics.mean(t_conf)
+    step_s = w.L * w.B * tl + w.B * tc
+    return w.B / step_s, {"lane_step_s": tl, "conf_s": tc, "timed_steps": len(t_lane),
+                          "step_s_extrapolated": step_s}
+
+
+def cpu_baseline(w, seconds):
+    value, info = oracle_sample(w, seconds)
+    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"single-threaded fp64 C++ oracle on 1 host core: one (layer, sequence) "
+                       f"lane of the same workload for {info['timed_steps']} steady decode "
+                       f"steps ({info['lane_step_s'] * 1e3:.1f} ms/lane-step) + B confidences "
+                       f"({info['conf_s'] * 1e3:.1f} ms each), extrapolated to L*B lanes "
+                       f"per step"),
+            "host": host_cpu()}
+
+
+def host_cpu():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return f"{line.split(':', 1)[1].strip()}, nproc={os.cpu_count()}"
+    except Exception:
+        pass
+    return f"nproc={os.cpu_count()}"
+
+
+# ---------------------------------------------------------------------------
+
+def attention_traffic():
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    capture, or None when the kernel source changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        sha = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()
+        if rec.get("kernel_sha256") == sha:
+            return rec["dram_bytes_per_launch_full_size"]
+    except Exception:
+        pass
+    return None
+
+
+def dist_setup(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allmax(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from synth import workloads as wl
+    w = get_workload(args)
+    # each timed step: a bounded sample of that decode step, extrapolated
+    import numpy as np
+
+    import oracle
+    o = oracle.Oracle.for_workload(w)
+    mask = np.zeros((w.L, w.B), np.uint8)
+    lane = (w.L // 2, w.B // 2)
+    mask[lane] = 1
+    o.set_active(mask)
+    if w.prefill:
+        k, v = wl.prefill_kv_lb(w, *lane)
+        o.prefill_lb(lane[0], lane[1], k, v, wl.q_last_lb(w, *lane))
+    else:
+        o.set_position(0)
+    total = 0.0
+    timed = 0
+    for s in range(args.warmup + args.steps):
+        lg, q, kn, vn = wl.step_inputs_lane(w, s, *lane)
+        t0 = time.perf_counter()
+        o.step(lg, q, kn, vn)
+        t1 = time.perf_counter()
+        if s >= args.warmup:
+            # lane-step time (confidences included) x L*B lanes
+            total += (t1 - t0) * w.L * w.B
+            timed += 1
+    value = w.B * timed / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total / max(timed, 1) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": ("each step: the oracle's decode step of one (layer, "
+                                        "sequence) lane (plus all B confidences), timed and "
+                                        "extrapolated x L*B"), "host": host_cpu()},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import confidence_gated_kv_logits_gb300 as pkg
+    from synth import device as sd, workloads as wl
+
+    ws, rank, local = dist_setup(args)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = get_workload(args)
+    K, Wm = args.steps, args.warmup
+    S = K + Wm
+
+    # ---- device-timed run ----
+    kv = pkg.ConfKV.for_workload(w)
+    if w.prefill:
+        Kp, Vp = sd.prefill_kv(w)
+        ql = wl.q_last(w)
+        kv.prefill(Kp, Vp, w.prefill, None if ql is None else torch.from_numpy(ql).to(dev))
+        torch.cuda.synchronize()
+        del Kp, Vp
+        torch.cuda.empty_cache()
+    LG = torch.empty(S, w.B, w.V, dtype=torch.float32, device=dev)
+    Q = torch.empty(S, w.L, w.B, w.Hq, w.d, dtype=torch.float16, device=dev)
+    KN = torch.empty(S, w.L, w.B, w.Hkv, w.d, dtype=torch.float16, device=dev)
+    VN = torch.empty(S, w.L, w.B, w.Hkv, w.d, dtype=torch.float16, device=dev)
+    for s in range(S):
+        sd.step_inputs(w, s, (LG[s], Q[s], KN[s], VN[s]))
+    out = torch.empty(w.L, w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+    kp = torch.empty(w.L, w.B, kv.Ncap, dtype=torch.int32, device=dev)
+    kc = torch.empty(w.L, w.B, dtype=torch.int32, device=dev)
+    cf = torch.empty(w.B, dtype=torch.float32, device=dev)
+    bd = torch.empty(w.B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    for s in range(Wm):
+        kv.step(LG[s], Q[s], KN[s], VN[s], out, kp, kc, cf, bd)
+    st0, _ = kv.stats()
+    kv.profile(["attention"])
+    clocks = ClockSampler(local)
+    time.sleep(0.15)
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    e0.record(stream)
+    for s in range(Wm, S):
+        kv.step(LG[s], Q[s], KN[s], VN[s], out, kp, kc, cf, bd)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(ws)
+    torch.cuda.synchronize()
+    time.sleep(0.1)
+    clocks.stop()
+    ms = e0.elapsed_time(e1)
+    prof = kv.profile_read()
+    kv.profile(())
+    st1, rc = kv.stats()
+    ms_max = allmax(ms, ws)
+    value = ws * w.B * K / (ms_max / 1e3)
+    attn_launches, attn_ms = prof["attention"]
+    attn_bytes = st1["attn_kv_bytes"] - st0["attn_kv_bytes"]
+    logit_bytes = st1["logits_bytes"] - st0["logits_bytes"]
+    hbm, peak_kind = peaks()
+    achieved = (attn_bytes / attn_launches) / (attn_ms / attn_launches / 1e3) / 1e9
+    pipe = (attn_bytes + logit_bytes) / (ms / 1e3) / 1e9
+    hi_frac = (st1["budget_high_steps"] - st0["budget_high_steps"]) / (K * w.B)
+    del LG, Q, KN, VN
+    kv.close()
+    torch.cuda.empty_cache()
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        Ke = min(K, args.e2e_steps)
+        kv = pkg.ConfKV.for_workload(w)
+        if w.prefill:
+            Kp, Vp = sd.prefill_kv(w)
+            ql = wl.q_last(w)
+            kv.prefill(Kp, Vp, w.prefill, None if ql is None else torch.from_numpy(ql).to(dev))
+            del Kp, Vp
+            torch.cuda.empty_cache()
+        bufs = (torch.empty(w.B, w.V, dtype=torch.float32, device=dev),
+                torch.empty(w.L, w.B, w.Hq, w.d, dtype=torch.float16, device=dev),
+                torch.empty(w.L, w.B, w.Hkv, w.d, dtype=torch.float16, device=dev),
+                torch.empty(w.L, w.B, w.Hkv, w.d, dtype=torch.float16, device=dev))
+        for s in range(Wm):
+            sd.step_inputs(w, s, bufs)
+            kv.step(*bufs, out, kp, kc, cf, bd)
+        host_in = []
+        for s in range(Wm, Wm + Ke):
+            sd.step_inputs(w, s, bufs)
+            host_in.append(tuple(x.cpu().pin_memory().numpy() for x in bufs))
+        h_out = torch.empty(w.L, w.B, w.Hq, w.d, dtype=torch.float32).pin_memory().numpy()
+        h_kp = torch.empty(w.L, w.B, kv.Ncap, dtype=torch.int32).pin_memory().numpy()
+        h_kc = torch.empty(w.L, w.B, dtype=torch.int32).pin_memory().numpy()
+        h_cf = torch.empty(w.B, dtype=torch.float32).pin_memory().numpy()
+        h_bd = torch.empty(w.B, dtype=torch.int32).pin_memory().numpy()
+        torch.cuda.synchronize()
+        barrier(ws)
+        t0 = time.perf_counter()
+        for s in range(Ke):
+            kv.step_host(*host_in[s], h_out, h_kp, h_kc, h_cf, h_bd)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        barrier(ws)
+        e2e_s = allmax(t1 - t0, ws)
+        h2d = sum(a.nbytes for a in host_in[0])
+        d2h = h_out.nbytes + h_kp.nbytes + h_kc.nbytes + h_cf.nbytes + h_bd.nbytes
+        e2e = {"value": ws * w.B * Ke / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": Ke,
+               "note": "confkv_step_host: pinned host inputs copied in, outputs (attention "
+                       "output, kept lists, c, budgets) copied out, every step"}
+        kv.close()
+        del host_in
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+            "warmup": Wm, "ms_per_step": ms_max / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 (fp16 + int8 KV storage, fp32 accumulate)", "data": "synthetic",
+            "config": workload_config(w, {"parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
+                                          "decode_steps": S}),
+            "roofline": {"bound": "hbm", "kernel": "attention (k_attn)",
+                         "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "peak_kind": f"{peak_kind} HBM copy",
+                         "traffic": attention_traffic(),
+                         "alg_bytes_per_launch": attn_bytes / attn_launches,
+                         "avg_launch_ms": attn_ms / attn_launches},
+            "pipeline": {"alg_bytes_per_step": (attn_bytes + logit_bytes) / K,
+                         "achieved_gbs": pipe, "frac": pipe / hbm,
+                         "attention_share_of_step": attn_ms / ms},
+            "budget_high_fraction": hi_frac,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 4 * K,
+            "clocks": clocks.summary(wall0, wall1),
+            "status": rc,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

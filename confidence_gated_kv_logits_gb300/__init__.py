@@ -237,8 +237,14 @@ class ConfKV:
         r["n8"], r["n16"] = a, c
         return r
 
-    def profile(self, enable):
-        self._check(self._L.confkv_profile_enable(self._h, 1 if enable else 0))
+    KERNELS = ("confidence", "select", "compact", "attention")
+
+    def profile(self, kernels=()):
+        """Time the named kernels with CUDA events (empty: off)."""
+        mask = 0
+        for k in kernels:
+            mask |= 1 << self.KERNELS.index(k)
+        self._check(self._L.confkv_profile_enable(self._h, mask))
 
     def profile_read(self):
         p = Profile()

@@ -67,7 +67,7 @@ struct confkv_ctx {
   int32_t* st_bud = nullptr;
   std::string msg = "ok";
   // profiling
-  bool prof = false;
+  int prof = 0;                                 // kernel bit mask
   std::vector<cudaEvent_t> ev[kProfKernels];   // start/stop pairs
   double prof_ms[kProfKernels] = {0, 0, 0, 0};
   long long prof_n[kProfKernels] = {0, 0, 0, 0};
@@ -109,7 +109,7 @@ int layer_budget(int N, int l, int L, double pmin, int P) {
 }
 
 void prof_mark(confkv_ctx* c, int k, cudaStream_t s) {
-  if (!c->prof) return;
+  if (!(c->prof & (1 << k))) return;
   cudaEvent_t e;
   if (cudaEventCreate(&e) != cudaSuccess) return;
   cudaEventRecord(e, s);
@@ -472,17 +472,13 @@ int confkv_read_cache(confkv_ctx* c, int l, int b, int cap, int* n8o, int* n16o,
   return CONFKV_OK;
 }
 
-int confkv_profile_enable(confkv_ctx* c, int enable) {
-  if (!c) return CONFKV_ERR_INVALID_ARG;
+int confkv_profile_enable(confkv_ctx* c, int kernel_mask) {
+  if (!c || kernel_mask < 0) return CONFKV_ERR_INVALID_ARG;
   DeviceGuard guard(c->device);
-  if (!enable && c->prof) {
-    cudaDeviceSynchronize();
-    prof_collect(c);
-  }
-  if (enable && !c->prof) {
-    for (int k = 0; k < kProfKernels; ++k) { c->prof_ms[k] = 0.0; c->prof_n[k] = 0; }
-  }
-  c->prof = enable != 0;
+  cudaDeviceSynchronize();
+  prof_collect(c);
+  for (int k = 0; k < kProfKernels; ++k) { c->prof_ms[k] = 0.0; c->prof_n[k] = 0; }
+  c->prof = kernel_mask & ((1 << kProfKernels) - 1);
   return CONFKV_OK;
 }
 

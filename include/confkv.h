@@ -190,8 +190,15 @@ int confkv_read_cache(confkv_ctx* ctx, int l, int b, int cap, int* n8, int* n16,
                       int32_t* pos, float* ema, int8_t* k8, int8_t* v8, float* ks,
                       float* vs, uint16_t* k16, uint16_t* v16, float* mass);
 
-/* Enable (1) / disable (0) per-kernel CUDA-event timing, and read it. */
-int confkv_profile_enable(confkv_ctx* ctx, int enable);
+/*
+ * Per-kernel CUDA-event timing of the step kernels (0 confidence, 1 select,
+ * 2 compact, 3 attention).  confkv_profile_enable(ctx, mask) synchronises,
+ * clears the totals and records an event pair around every launch of each
+ * kernel whose bit is set in `mask` (0 disables).  confkv_profile_read
+ * synchronises and returns launches and total milliseconds per kernel.
+ * Timing adds event records to the stream; leave it off in production.
+ */
+int confkv_profile_enable(confkv_ctx* ctx, int kernel_mask);
 int confkv_profile_read(confkv_ctx* ctx, confkv_profile_t* out);
 
 /* Message of the last error of this context (never NULL). */

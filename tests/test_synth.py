@@ -45,3 +45,12 @@ def test_prefill_slice_matches_full_tensor_and_needles():
         cos = np.sum(nk * u, -1) / np.linalg.norm(nk, axis=-1)
         assert np.all(cos > 0.999)
     assert wl.q_last(w).shape == (2, 2, 4, 8)
+
+
+def test_lane_inputs_match_full_inputs():
+    w = wl.QWEN32B.with_(L=3, B=2, V=500, prefill=100)
+    full = wl.step_inputs(w, 7)
+    lane = wl.step_inputs_lane(w, 7, 2, 1)
+    assert np.array_equal(full[0], lane[0])
+    for a, b in zip(full[1:], lane[1:]):
+        assert np.array_equal(a[2, 1], b[2, 1]) and not b[0].any()
