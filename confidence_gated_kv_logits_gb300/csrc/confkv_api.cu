@@ -41,8 +41,8 @@ struct DeviceGuard {
 
 struct confkv_ctx {
   int L = 0, B = 0, Hq = 0, Hkv = 0, d = 0, g = 0, V = 0;
-  int N_low = 0, N_high = 0, P = 0, W = 0, Ncap = 0, cap8 = 0, slots = 0;
-  int max_context = 0, device = 0, splits = 1;
+  int N_low = 0, N_high = 0, P = 0, W = 0, Wr = 0, Ncap = 0, cap8 = 0, slots = 0;
+  int max_context = 0, device = 0, splits = 1, attn_kernel = 0;
   float tau = 0.f, beta = 0.f, omb = 0.f, pyramid_min = 1.f;
   int64_t t = 0, steps = 0;
   bool prefilled = false;
@@ -135,6 +135,7 @@ int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s) {
   AttnParams ap{};
   ap.q = q;
   ap.out = out;
+  ap.kernel = c->attn_kernel;
   ap.splits = c->splits;
   ap.part_ml = c->part_ml;
   ap.part_acc = c->part_acc;
@@ -162,7 +163,9 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
       heads / kv_heads > confkv::kMaxGroup || (head_dim != 64 && head_dim != 128) || P < 1 ||
       W < P || N_low < P || N_high < P || !(ema_decay >= 0.0f && ema_decay <= 1.0f) ||
       !std::isfinite(tau) || o.batch < 1 || o.vocab < 2 || o.max_context < 0 ||
-      !(pmin > 0.0f && pmin <= 1.0f) || o.attn_splits < 0 || o.attn_splits > 64)
+      !(pmin > 0.0f && pmin <= 1.0f) || o.attn_splits < 0 || o.attn_splits > 64 ||
+      o.attn_kernel < 0 || o.attn_kernel > 2 ||
+      (o.attn_kernel == 2 && heads / kv_heads > 8))
     return CONFKV_ERR_INVALID_ARG;
   int dev = o.device;
   if (!opts || dev < 0) cudaGetDevice(&dev);
@@ -185,10 +188,12 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   c->pyramid_min = pmin;
   c->max_context = o.max_context;
   c->device = dev;
+  c->attn_kernel = o.attn_kernel;
   c->Ncap = std::max(N_low, N_high);
   c->cap8 = std::max(std::max(0, o.max_context - W), c->Ncap);
-  c->cap8 = (c->cap8 + 15) / 16 * 16;
-  c->slots = c->cap8 + W;
+  c->cap8 = (c->cap8 + 31) / 32 * 32;
+  c->Wr = (W + 15) / 16 * 16;
+  c->slots = c->cap8 + c->Wr;
 
   const size_t LB = static_cast<size_t>(c->L) * c->B;
   const size_t U = LB * c->Hkv;
@@ -203,26 +208,26 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
 
   Cache& k = c->cache;
   k.L = c->L; k.B = c->B; k.Hq = c->Hq; k.Hkv = c->Hkv; k.d = c->d; k.g = c->g;
-  k.W = c->W; k.P = c->P; k.cap8 = c->cap8; k.slots = c->slots; k.Ncap = c->Ncap;
+  k.W = c->W; k.Wr = c->Wr; k.P = c->P; k.cap8 = c->cap8; k.slots = c->slots; k.Ncap = c->Ncap;
   cudaError_t e = cudaSuccess;
   auto A = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
   A(dalloc(c, &k.k8, U * c->cap8 * c->d));
   A(dalloc(c, &k.v8, U * c->cap8 * c->d));
   A(dalloc(c, &k.ks, U * c->cap8));
   A(dalloc(c, &k.vs, U * c->cap8));
-  A(dalloc(c, &k.k16, U * c->W * c->d));
-  A(dalloc(c, &k.v16, U * c->W * c->d));
+  A(dalloc(c, &k.k16, U * c->Wr * c->d));
+  A(dalloc(c, &k.v16, U * c->Wr * c->d));
   A(dalloc(c, &k.pos8, LB * c->cap8));
-  A(dalloc(c, &k.pos16, LB * c->W));
+  A(dalloc(c, &k.pos16, LB * c->Wr));
   A(dalloc(c, &k.ema8, LB * c->cap8));
-  A(dalloc(c, &k.ema16, LB * c->W));
+  A(dalloc(c, &k.ema16, LB * c->Wr));
   A(dalloc(c, &k.mass, U * c->slots));
   A(dalloc(c, &k.scores, LB * c->Hq * c->slots));
   A(dalloc(c, &k.keys, LB * c->slots));
   A(dalloc(c, &k.n8, LB));
   A(dalloc(c, &k.n16, LB));
   A(dalloc(c, &k.jobs8, LB * c->cap8));
-  A(dalloc(c, &k.jobs16, LB * c->W));
+  A(dalloc(c, &k.jobs16, LB * c->Wr));
   A(dalloc(c, &k.njobs, LB * 2));
   A(dalloc(c, &k.stats, 1));
   A(dalloc(c, &k.err, 1));
@@ -426,11 +431,11 @@ int confkv_read_cache(confkv_ctx* c, int l, int b, int cap, int* n8o, int* n16o,
   };
   if (pos) {
     cp(pos, c->cache.pos8 + lb * c->cap8, r8 * 4);
-    cp(pos + r8, c->cache.pos16 + lb * c->W, r16 * 4);
+    cp(pos + r8, c->cache.pos16 + lb * c->Wr, r16 * 4);
   }
   if (ema) {
     cp(ema, c->cache.ema8 + lb * c->cap8, r8 * 4);
-    cp(ema + r8, c->cache.ema16 + lb * c->W, r16 * 4);
+    cp(ema + r8, c->cache.ema16 + lb * c->Wr, r16 * 4);
   }
   std::vector<int8_t> t8(static_cast<size_t>(std::max(r8, 1)) * d);
   std::vector<float> tf(std::max(r8, 1));
@@ -451,7 +456,7 @@ int confkv_read_cache(confkv_ctx* c, int l, int b, int cap, int* n8o, int* n16o,
       }
       uint16_t* dst16 = which ? v16 : k16;
       if (dst16 && r16) {
-        cp(t16.data(), reinterpret_cast<const uint16_t*>(which ? c->cache.v16 : c->cache.k16) + u * c->W * d,
+        cp(t16.data(), reinterpret_cast<const uint16_t*>(which ? c->cache.v16 : c->cache.k16) + u * c->Wr * d,
            static_cast<size_t>(r16) * d * 2);
         for (int i = 0; i < r16; ++i)
           std::memcpy(dst16 + (static_cast<size_t>(i) * H + h) * d, t16.data() + static_cast<size_t>(i) * d, d * 2);

@@ -3,11 +3,12 @@
 // HBM layout of one context (lb = l*B + b, h = KV head):
 //   INT8 region   k8, v8  int8  [L*B][Hkv][cap8][d]    (slots 0..n8-1 live)
 //                 ks, vs  fp32  [L*B][Hkv][cap8]       one absmax scale per row
-//   FP16 region   k16,v16 fp16  [L*B][Hkv][W][d]       (slots 0..n16-1 live)
-//   metadata      pos8, ema8 [L*B][cap8]; pos16, ema16 [L*B][W]
+//   FP16 region   k16,v16 fp16  [L*B][Hkv][Wr][d]      (slots 0..n16-1 live;
+//                 Wr = W rounded up to 16, so whole 16-token chunks stay in bounds)
+//   metadata      pos8, ema8 [L*B][cap8]; pos16, ema16 [L*B][Wr]   (cap8 % 32 == 0)
 //   mass          fp32 [L*B][Hkv][slots]   attention mass of the last
 //                 attention summed over the query heads of one KV head;
-//                 slot id = INT8 slot, or cap8 + FP16 slot; slots = cap8 + W
+//                 slot id = INT8 slot, or cap8 + FP16 slot; slots = cap8 + Wr
 //   scores        fp32 [L*B][Hq][slots]    raw scores of the last attention
 // Both regions are dense (contiguous compaction): live slots are always
 // [0, n8) and [0, n16), so the attention streams them without any indirection.
@@ -31,7 +32,7 @@ struct DevStats {
 };
 
 struct Cache {
-  int L, B, Hq, Hkv, d, g, W, P, cap8, slots, Ncap;
+  int L, B, Hq, Hkv, d, g, W, Wr, P, cap8, slots, Ncap;
   int8_t* k8;
   int8_t* v8;
   float* ks;
@@ -48,7 +49,7 @@ struct Cache {
   int32_t* n8;
   int32_t* n16;
   int2* jobs8;      // [L*B][cap8]  (dst INT8 slot, src INT8 slot)
-  int2* jobs16;     // [L*B][W]     (dst FP16 slot, src FP16 slot or -1 = new token)
+  int2* jobs16;     // [L*B][Wr]     (dst FP16 slot, src FP16 slot or -1 = new token)
   int32_t* njobs;   // [L*B][2]     INT8 moves, FP16 writes
   DevStats* stats;
   int32_t* err;
@@ -64,6 +65,7 @@ struct StepParams {
 };
 
 struct AttnParams {
+  int kernel;             // 0 auto, 1 CUDA-core, 2 tensor-core
   const __half* q;       // [L*B][Hq][d]
   float* out;            // [L*B][Hq][d]
   int splits;
@@ -84,5 +86,6 @@ cudaError_t launch_compact(const Cache& c, const __half* k_new, const __half* v_
 cudaError_t launch_prefill_store(const Cache& c, const __half* k, const __half* v, int T,
                                  cudaStream_t s);
 cudaError_t launch_attention(const Cache& c, const AttnParams& ap, cudaStream_t s);
+cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStream_t s);
 
 }  // namespace confkv

@@ -76,8 +76,8 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
   const int8_t* V8 = c.v8 + static_cast<size_t>(unit) * c.cap8 * D;
   const float* KS = c.ks + static_cast<size_t>(unit) * c.cap8;
   const float* VS = c.vs + static_cast<size_t>(unit) * c.cap8;
-  const __half* K16 = c.k16 + static_cast<size_t>(unit) * c.W * D;
-  const __half* V16 = c.v16 + static_cast<size_t>(unit) * c.W * D;
+  const __half* K16 = c.k16 + static_cast<size_t>(unit) * c.Wr * D;
+  const __half* V16 = c.v16 + static_cast<size_t>(unit) * c.Wr * D;
   float* SC = c.scores + (static_cast<size_t>(lb) * c.Hq + kvh * g) * c.slots;
 
   for (int tile = t0 + warp; tile < t1; tile += kWarps) {
@@ -253,6 +253,9 @@ cudaError_t launch_simple(const Cache& c, const AttnParams& ap, cudaStream_t s) 
 }  // namespace
 
 cudaError_t launch_attention(const Cache& c, const AttnParams& ap, cudaStream_t s) {
+  const bool mma_ok = c.g >= 1 && c.g <= 8;
+  if (ap.kernel == 2 && !mma_ok) return cudaErrorInvalidValue;
+  if (ap.kernel != 1 && mma_ok) return launch_attention_mma(c, ap, s);
   if (c.d == 64) return launch_simple<64>(c, ap, s);
   if (c.d == 128) return launch_simple<128>(c, ap, s);
   return cudaErrorInvalidValue;

@@ -1,0 +1,557 @@
+// K4 (tensor-core path): split-K decode attention over the INT8 and FP16
+// regions for GQA groups of 1..8 query heads per KV head, with the INT8
+// dequantisation fused into the block reads.
+//
+// CONF-KV page, Technische Samenvatting:
+//   Implementatie  dequantisation is fused with block-wise attention reads;
+//     the compacted (dense) cache is streamed without indirection tables.
+//   Systeemontwerp  block-wise online-softmax attention over mixed FP16/INT8.
+//   Tokenrangschikking  the per-token attention mass feeds the next EMA.
+//
+// Arithmetic per 16-token block (mma.sync m16n8k16, fp16 in, fp32 accumulate):
+//   S^T[tok][q] = K[tok][:] . Q[q][:]      M = 16 tokens, N = 8 query slots,
+//                                          K = head_dim (permuted, see below)
+//   O^T[d][q]  += V^T[d][tok] . P'^T[tok][q]    M = 16 channels, K = 16 tokens
+// INT8 codes become fp16 exactly (byte | 0x6400 is 1024 + byte; minus 1152).
+// The K scale multiplies the score row; the V scale is folded into P' = p*vs.
+// P' is split into fp16 hi + lo (two MMAs), scaled by a per-chunk power of
+// two so that it stays in fp16's normal range: the rounding of P' is ~2^-22
+// relative, well inside the 1e-3 output tolerance.  P' is moved from the
+// score layout to the B-operand layout with movmatrix.trans.
+//
+// The contraction index of Q.K^T is permuted so that each thread reads one
+// contiguous slice of a K row (32 B of INT8 at d = 128); the M index of the
+// P.V product is permuted so that each thread reads one contiguous slice of
+// a V row.  Each warp streams its own chunks (32 INT8 tokens or 16 FP16
+// tokens, 8 KB at d = 128) through a cp.async ring of kStages stages in a
+// thread-private shared-memory layout (conflict-free, no cross-lane data
+// except the 64 scales of an INT8 chunk).
+#include <cfloat>
+
+#include "confkv_internal.cuh"
+
+namespace confkv {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;
+constexpr uint32_t kBias = 0x80808080u;     // int8 -> biased uint8
+constexpr uint32_t kMagic = 0x64646464u;    // fp16 exponent byte of 1024
+constexpr uint32_t kH1152 = 0x64806480u;    // half2(1152, 1152)
+
+template <int D>
+struct Geo {
+  static constexpr int KPT = D / 4;          // K channels per thread per row
+  static constexpr int VPT = D / 8;          // V channels per thread per row
+  static constexpr int KS = D / 16;          // k-steps of S, m-tiles of O
+  static constexpr int UNITS = D / 8;        // 16-byte units per thread per chunk
+  static constexpr int DATA = UNITS * 32 * 16;
+  static constexpr int STAGE = DATA + 256;   // + 32 K scales + 32 V scales
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// thread-private byte offset b of a stage -> shared address
+__device__ __forceinline__ uint32_t tp(uint32_t stage, int lane, int b) {
+  return stage + static_cast<uint32_t>(((b >> 4) * 32 + lane) * 16 + (b & 15));
+}
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float ldsf(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+// two biased int8 bytes of w (selected by sel) -> exact half2
+__device__ __forceinline__ uint32_t i8h2(uint32_t w_biased, uint32_t sel) {
+  uint32_t r = __byte_perm(w_biased, kMagic, sel);
+  uint32_t m = kH1152;
+  __half2 h = __hsub2(*reinterpret_cast<__half2*>(&r), *reinterpret_cast<__half2*>(&m));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_h2(__half a, __half b) {
+  __half2 h = __halves2half2(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float gmax8(float v) {   // max over the 8 lanes sharing t4
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+}
+__device__ __forceinline__ float gsum8(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  return v + __shfl_xor_sync(0xffffffffu, v, 16);
+}
+__device__ __forceinline__ float rescale(float m_old, float m_new) {
+  return (m_old == -INFINITY) ? 0.0f : expf(m_old - m_new);
+}
+
+// cp.async of one chunk into a stage.  INT8 chunk ci: slots 32ci..32ci+31
+// (two 16-token blocks); FP16 chunk: slots 16cf..16cf+15.
+template <int D>
+__device__ __forceinline__ void issue_chunk(const Cache& c, int unit, int nc8, int ci,
+                                            uint32_t st, int lane) {
+  using G = Geo<D>;
+  const int gid = lane >> 2, t4 = lane & 3;
+  if (ci < nc8) {
+    const size_t row0 = static_cast<size_t>(unit) * c.cap8 + 32 * ci;
+    const int8_t* K8 = c.k8 + row0 * D;
+    const int8_t* V8 = c.v8 + row0 * D;
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int tok = 16 * sb + gid + 8 * r;
+#pragma unroll
+        for (int p = 0; p < G::KPT / 16; ++p)
+          cp16(tp(st, lane, (2 * sb + r) * G::KPT + 16 * p), K8 + tok * D + t4 * G::KPT + 16 * p);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int tok = 16 * sb + 2 * t4 + (i & 1) + 8 * (i >> 1);
+        const int b = D + (4 * sb + i) * G::VPT;
+        if constexpr (G::VPT == 16) cp16(tp(st, lane, b), V8 + tok * D + gid * G::VPT);
+        else cp8(tp(st, lane, b), V8 + tok * D + gid * G::VPT);
+      }
+    }
+    if (lane < 16) {
+      const float* S = (lane < 8 ? c.ks : c.vs) + row0 + 4 * (lane & 7);
+      cp16(st + G::DATA + 16 * lane, S);
+    }
+  } else {
+    const size_t row0 = static_cast<size_t>(unit) * c.Wr + 16 * (ci - nc8);
+    const char* K16 = reinterpret_cast<const char*>(c.k16 + row0 * D);
+    const char* V16 = reinterpret_cast<const char*>(c.v16 + row0 * D);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int tok = gid + 8 * r;
+#pragma unroll
+      for (int p = 0; p < G::KPT * 2 / 16; ++p)
+        cp16(tp(st, lane, r * G::KPT * 2 + 16 * p), K16 + (tok * D + t4 * G::KPT) * 2 + 16 * p);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int tok = 2 * t4 + (i & 1) + 8 * (i >> 1);
+#pragma unroll
+      for (int p = 0; p < G::VPT * 2 / 16; ++p)
+        cp16(tp(st, lane, D + i * G::VPT * 2 + 16 * p), V16 + (tok * D + gid * G::VPT) * 2 + 16 * p);
+    }
+  }
+}
+
+struct SoftState {
+  float mA, mB, lA, lB;   // queries 2*t4 (A) and 2*t4+1 (B)
+  int E;                  // O holds values scaled by 2^E
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap) {
+  using G = Geo<D>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int unit = blockIdx.x, split = blockIdx.y;
+  const int lb = unit / c.Hkv, kvh = unit - lb * c.Hkv, g = c.g;
+  const int n8 = c.n8[lb], n16 = c.n16[lb], n = n8 + n16;
+  const int nc8 = (n8 + 31) >> 5, nc16 = (n16 + 15) >> 4, nc = nc8 + nc16;
+  const int cb = static_cast<int>(static_cast<long long>(nc) * split / ap.splits);
+  const int ce = static_cast<int>(static_cast<long long>(nc) * (split + 1) / ap.splits);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, t4 = lane & 3;
+  const int cnt = (ce - cb > warp) ? (ce - cb - warp + kWarps - 1) / kWarps : 0;
+  const uint32_t wbase = smem_u32(smem) + warp * kStages * G::STAGE;
+  const float* fbase = reinterpret_cast<const float*>(smem + warp * kStages * G::STAGE);
+
+  // Q^T operand: query gid, channels t4*KPT + 4kk + {0,1} and {2,3}
+  uint32_t qb[G::KS][2];
+  if (gid < g) {
+    const uint4* qp = reinterpret_cast<const uint4*>(
+        ap.q + (static_cast<size_t>(lb) * c.Hq + kvh * g + gid) * D + t4 * G::KPT);
+#pragma unroll
+    for (int j = 0; j < G::KS / 2; ++j) {
+      const uint4 v = qp[j];
+      qb[2 * j][0] = v.x;
+      qb[2 * j][1] = v.y;
+      qb[2 * j + 1][0] = v.z;
+      qb[2 * j + 1][1] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < G::KS; ++kk) qb[kk][0] = qb[kk][1] = 0u;
+  }
+
+  float O[G::KS][4];
+#pragma unroll
+  for (int mt = 0; mt < G::KS; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.0f;
+  SoftState ss{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
+  float* SC = c.scores + (static_cast<size_t>(lb) * c.Hq + kvh * g) * c.slots;
+  const bool wA = 2 * t4 < g, wB = 2 * t4 + 1 < g;
+
+  // one online-softmax update with a new scale exponent; returns 2^E
+  auto update = [&](float mxA, float mxB, int Enew) -> float {
+    mxA = gmax8(mxA);
+    mxB = gmax8(mxB);
+    const float nA = fmaxf(ss.mA, mxA), nB = fmaxf(ss.mB, mxB);
+    const float f = ldexpf(1.0f, Enew - ss.E);
+    const float cA = rescale(ss.mA, nA), cB = rescale(ss.mB, nB);
+    ss.lA *= cA;
+    ss.lB *= cB;
+    const float fA = cA * f, fB = cB * f;
+#pragma unroll
+    for (int mt = 0; mt < G::KS; ++mt) {
+      O[mt][0] *= fA;
+      O[mt][2] *= fA;
+      O[mt][1] *= fB;
+      O[mt][3] *= fB;
+    }
+    ss.mA = nA;
+    ss.mB = nB;
+    ss.E = Enew;
+    return ldexpf(1.0f, Enew);
+  };
+  // P' (4 values of the score layout) -> hi/lo B operands, then P'.V MMAs
+  auto pv_int8 = [&](const float (&x)[4], const uint32_t (&vw)[4][G::VPT / 4]) {
+    const __half h0 = __float2half_rn(x[0]), h1 = __float2half_rn(x[1]);
+    const __half h2 = __float2half_rn(x[2]), h3 = __float2half_rn(x[3]);
+    const uint32_t bh0 = movtrans(pack_h2(h0, h1)), bh1 = movtrans(pack_h2(h2, h3));
+    const uint32_t bl0 = movtrans(pack_h2(__float2half_rn(x[0] - __half2float(h0)),
+                                          __float2half_rn(x[1] - __half2float(h1))));
+    const uint32_t bl1 = movtrans(pack_h2(__float2half_rn(x[2] - __half2float(h2)),
+                                          __float2half_rn(x[3] - __half2float(h3))));
+#pragma unroll
+    for (int mt = 0; mt < G::KS; ++mt) {
+      const int w = mt >> 1;
+      const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+      const uint32_t p01 = __byte_perm(vw[0][w], vw[1][w], sel) ^ kBias;
+      const uint32_t p23 = __byte_perm(vw[2][w], vw[3][w], sel) ^ kBias;
+      const uint32_t a[4] = {i8h2(p01, 0x4140u), i8h2(p01, 0x4342u), i8h2(p23, 0x4140u),
+                             i8h2(p23, 0x4342u)};
+      mma16816(O[mt], a, bh0, bh1);
+      mma16816(O[mt], a, bl0, bl1);
+    }
+  };
+  auto pv_f16 = [&](const float (&x)[4], const uint32_t (&vw)[4][G::VPT / 2]) {
+    const __half h0 = __float2half_rn(x[0]), h1 = __float2half_rn(x[1]);
+    const __half h2 = __float2half_rn(x[2]), h3 = __float2half_rn(x[3]);
+    const uint32_t bh0 = movtrans(pack_h2(h0, h1)), bh1 = movtrans(pack_h2(h2, h3));
+    const uint32_t bl0 = movtrans(pack_h2(__float2half_rn(x[0] - __half2float(h0)),
+                                          __float2half_rn(x[1] - __half2float(h1))));
+    const uint32_t bl1 = movtrans(pack_h2(__float2half_rn(x[2] - __half2float(h2)),
+                                          __float2half_rn(x[3] - __half2float(h3))));
+#pragma unroll
+    for (int mt = 0; mt < G::KS; ++mt) {
+      const uint32_t a[4] = {__byte_perm(vw[0][mt], vw[1][mt], 0x5410u),
+                             __byte_perm(vw[0][mt], vw[1][mt], 0x7632u),
+                             __byte_perm(vw[2][mt], vw[3][mt], 0x5410u),
+                             __byte_perm(vw[2][mt], vw[3][mt], 0x7632u)};
+      mma16816(O[mt], a, bh0, bh1);
+      mma16816(O[mt], a, bl0, bl1);
+    }
+  };
+
+  // ---- main loop over this warp's chunks ----
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) {
+    if (i < cnt) issue_chunk<D>(c, unit, nc8, cb + warp + kWarps * i, wbase + i * G::STAGE, lane);
+    cp_commit();
+  }
+  for (int i = 0; i < cnt; ++i) {
+    cp_wait<kStages - 2>();
+    __syncwarp();
+    {
+      const int nx = i + kStages - 1;
+      if (nx < cnt)
+        issue_chunk<D>(c, unit, nc8, cb + warp + kWarps * nx, wbase + (nx % kStages) * G::STAGE, lane);
+      cp_commit();
+    }
+    const int ci = cb + warp + kWarps * i;
+    const int sidx = i % kStages;
+    const uint32_t st = wbase + sidx * G::STAGE;
+    if (ci < nc8) {
+      // ------------------------- INT8 chunk: 32 tokens -------------------------
+      const float* sks = fbase + (sidx * G::STAGE + G::DATA) / 4;
+      const float* svs = sks + 32;
+      const int tb = 32 * ci;
+      float s[2][4];
+      float vmax = 0.0f;
+#pragma unroll
+      for (int sb = 0; sb < 2; ++sb) {
+        uint32_t kw[2][G::KS];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int u = 0; u < G::KPT / 16; ++u) {
+            const uint4 v = lds128(tp(st, lane, (2 * sb + r) * G::KPT + 16 * u));
+            kw[r][4 * u] = v.x;
+            kw[r][4 * u + 1] = v.y;
+            kw[r][4 * u + 2] = v.z;
+            kw[r][4 * u + 3] = v.w;
+          }
+        s[sb][0] = s[sb][1] = s[sb][2] = s[sb][3] = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < G::KS; ++kk) {
+          const uint32_t w0 = kw[0][kk] ^ kBias, w1 = kw[1][kk] ^ kBias;
+          const uint32_t a[4] = {i8h2(w0, 0x4140u), i8h2(w1, 0x4140u), i8h2(w0, 0x4342u),
+                                 i8h2(w1, 0x4342u)};
+          mma16816(s[sb], a, qb[kk][0], qb[kk][1]);
+        }
+        const int t0 = tb + 16 * sb + gid, t1 = t0 + 8;
+        const bool v0 = t0 < n8, v1 = t1 < n8;
+        const float k0 = sks[16 * sb + gid] * ap.scale, k1 = sks[16 * sb + gid + 8] * ap.scale;
+        s[sb][0] = v0 ? s[sb][0] * k0 : -INFINITY;
+        s[sb][1] = v0 ? s[sb][1] * k0 : -INFINITY;
+        s[sb][2] = v1 ? s[sb][2] * k1 : -INFINITY;
+        s[sb][3] = v1 ? s[sb][3] * k1 : -INFINITY;
+        if (wA) {
+          if (v0) SC[static_cast<size_t>(2 * t4) * c.slots + t0] = s[sb][0];
+          if (v1) SC[static_cast<size_t>(2 * t4) * c.slots + t1] = s[sb][2];
+        }
+        if (wB) {
+          if (v0) SC[static_cast<size_t>(2 * t4 + 1) * c.slots + t0] = s[sb][1];
+          if (v1) SC[static_cast<size_t>(2 * t4 + 1) * c.slots + t1] = s[sb][3];
+        }
+        if (v0) vmax = fmaxf(vmax, svs[16 * sb + gid]);
+        if (v1) vmax = fmaxf(vmax, svs[16 * sb + gid + 8]);
+      }
+      vmax = gmax8(vmax);
+      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+      int e = 0;
+      frexpf(vmax, &e);
+      const int Enew = (vmax > 0.0f) ? max(-60, min(60, 14 - e)) : ss.E;
+      const float two = update(fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2])),
+                               fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3])), Enew);
+#pragma unroll
+      for (int sb = 0; sb < 2; ++sb) {
+        const float pA0 = expf(s[sb][0] - ss.mA), pB0 = expf(s[sb][1] - ss.mB);
+        const float pA1 = expf(s[sb][2] - ss.mA), pB1 = expf(s[sb][3] - ss.mB);
+        ss.lA += pA0 + pA1;
+        ss.lB += pB0 + pB1;
+        const int t0 = tb + 16 * sb + gid;
+        const float vs0 = (t0 < n8) ? svs[16 * sb + gid] * two : 0.0f;
+        const float vs1 = (t0 + 8 < n8) ? svs[16 * sb + gid + 8] * two : 0.0f;
+        const float x[4] = {pA0 * vs0, pB0 * vs0, pA1 * vs1, pB1 * vs1};
+        uint32_t vw[4][G::VPT / 4];
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+          const int b = D + (4 * sb + ii) * G::VPT;
+          if constexpr (G::VPT == 16) {
+            const uint4 v = lds128(tp(st, lane, b));
+            vw[ii][0] = v.x;
+            vw[ii][1] = v.y;
+            vw[ii][2] = v.z;
+            vw[ii][3] = v.w;
+          } else {
+            const uint2 v = lds64(tp(st, lane, b));
+            vw[ii][0] = v.x;
+            vw[ii][1] = v.y;
+          }
+        }
+        pv_int8(x, vw);
+      }
+    } else {
+      // ------------------------- FP16 chunk: 16 tokens -------------------------
+      const int tb = 16 * (ci - nc8);
+      uint32_t kw[2][G::KPT / 2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int u = 0; u < G::KPT / 8; ++u) {
+          const uint4 v = lds128(tp(st, lane, r * G::KPT * 2 + 16 * u));
+          kw[r][4 * u] = v.x;
+          kw[r][4 * u + 1] = v.y;
+          kw[r][4 * u + 2] = v.z;
+          kw[r][4 * u + 3] = v.w;
+        }
+      float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int kk = 0; kk < G::KS; ++kk) {
+        const uint32_t a[4] = {kw[0][2 * kk], kw[1][2 * kk], kw[0][2 * kk + 1], kw[1][2 * kk + 1]};
+        mma16816(s, a, qb[kk][0], qb[kk][1]);
+      }
+      const int t0 = tb + gid, t1 = t0 + 8;
+      const bool v0 = t0 < n16, v1 = t1 < n16;
+      s[0] = v0 ? s[0] * ap.scale : -INFINITY;
+      s[1] = v0 ? s[1] * ap.scale : -INFINITY;
+      s[2] = v1 ? s[2] * ap.scale : -INFINITY;
+      s[3] = v1 ? s[3] * ap.scale : -INFINITY;
+      const size_t o0 = static_cast<size_t>(c.cap8) + t0, o1 = o0 + 8;
+      if (wA) {
+        if (v0) SC[static_cast<size_t>(2 * t4) * c.slots + o0] = s[0];
+        if (v1) SC[static_cast<size_t>(2 * t4) * c.slots + o1] = s[2];
+      }
+      if (wB) {
+        if (v0) SC[static_cast<size_t>(2 * t4 + 1) * c.slots + o0] = s[1];
+        if (v1) SC[static_cast<size_t>(2 * t4 + 1) * c.slots + o1] = s[3];
+      }
+      const float two = update(fmaxf(s[0], s[2]), fmaxf(s[1], s[3]), 13);
+      const float pA0 = expf(s[0] - ss.mA), pB0 = expf(s[1] - ss.mB);
+      const float pA1 = expf(s[2] - ss.mA), pB1 = expf(s[3] - ss.mB);
+      ss.lA += pA0 + pA1;
+      ss.lB += pB0 + pB1;
+      const float x[4] = {pA0 * two, pB0 * two, pA1 * two, pB1 * two};
+      uint32_t vw[4][G::VPT / 2];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int u = 0; u < G::VPT / 8; ++u) {
+          const uint4 v = lds128(tp(st, lane, D + ii * G::VPT * 2 + 16 * u));
+          vw[ii][4 * u] = v.x;
+          vw[ii][4 * u + 1] = v.y;
+          vw[ii][4 * u + 2] = v.z;
+          vw[ii][4 * u + 3] = v.w;
+        }
+      // zero the V rows of tokens past the region end (stale slots)
+      if (!(2 * t4 < n16 - tb)) { for (int u = 0; u < G::VPT / 2; ++u) vw[0][u] = 0u; }
+      if (!(2 * t4 + 1 < n16 - tb)) { for (int u = 0; u < G::VPT / 2; ++u) vw[1][u] = 0u; }
+      if (!(2 * t4 + 8 < n16 - tb)) { for (int u = 0; u < G::VPT / 2; ++u) vw[2][u] = 0u; }
+      if (!(2 * t4 + 9 < n16 - tb)) { for (int u = 0; u < G::VPT / 2; ++u) vw[3][u] = 0u; }
+      pv_f16(x, vw);
+    }
+  }
+  cp_wait<0>();
+
+  // ---- merge the warps of this CTA (shared memory reused) ----
+  ss.lA = gsum8(ss.lA);
+  ss.lB = gsum8(ss.lB);
+  __syncthreads();
+  float* wm = reinterpret_cast<float*>(smem);            // [kWarps][8]
+  float* wl = wm + kWarps * 8;                           // [kWarps][8]
+  float* fin = wl + kWarps * 8;                          // [2][8]
+  float* wo = fin + 16;                                  // [kWarps][8][D]
+  const float unscale = ldexpf(1.0f, -ss.E);
+  if (gid == 0) {
+    wm[warp * 8 + 2 * t4] = ss.mA;
+    wm[warp * 8 + 2 * t4 + 1] = ss.mB;
+    wl[warp * 8 + 2 * t4] = ss.lA;
+    wl[warp * 8 + 2 * t4 + 1] = ss.lB;
+  }
+#pragma unroll
+  for (int mt = 0; mt < G::KS; ++mt) {
+    const int d0 = gid * G::VPT + 2 * mt;
+    float* oa = wo + (warp * 8 + 2 * t4) * D;
+    float* ob = oa + D;
+    oa[d0] = O[mt][0] * unscale;
+    ob[d0] = O[mt][1] * unscale;
+    oa[d0 + 1] = O[mt][2] * unscale;
+    ob[d0 + 1] = O[mt][3] * unscale;
+  }
+  __syncthreads();
+  const size_t obase = static_cast<size_t>(lb) * c.Hq + kvh * g;
+  for (int idx = tid; idx < g * D; idx += kThreads) {
+    const int h = idx / D, dd = idx - h * D;
+    float M = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 8 + h]);
+    float Ls = 0.0f, A = 0.0f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = rescale(wm[w * 8 + h], M);
+      Ls += wl[w * 8 + h] * f;
+      A += wo[(w * 8 + h) * D + dd] * f;
+    }
+    if (ap.splits == 1) {
+      ap.out[(obase + h) * D + dd] = A / Ls;
+      if (dd == 0) { fin[h] = M; fin[8 + h] = Ls; }
+    } else {
+      const size_t pi = (obase + h) * ap.splits + split;
+      ap.part_acc[pi * D + dd] = A;
+      if (dd == 0) { ap.part_ml[pi * 2] = M; ap.part_ml[pi * 2 + 1] = Ls; }
+    }
+  }
+  int tok_lo = 0, tok_hi = 0;   // unified token range whose mass this CTA writes
+  if (ap.splits == 1) {
+    tok_hi = n;
+  } else {
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(&ap.ticket[unit], 1u) == static_cast<unsigned>(ap.splits - 1));
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int idx = tid; idx < g * D; idx += kThreads) {
+      const int h = idx / D, dd = idx - h * D;
+      const size_t pb = (obase + h) * ap.splits;
+      float M = -INFINITY;
+      for (int sp = 0; sp < ap.splits; ++sp) M = fmaxf(M, __ldcg(&ap.part_ml[(pb + sp) * 2]));
+      float Ls = 0.0f, A = 0.0f;
+      for (int sp = 0; sp < ap.splits; ++sp) {
+        const float f = rescale(__ldcg(&ap.part_ml[(pb + sp) * 2]), M);
+        Ls += __ldcg(&ap.part_ml[(pb + sp) * 2 + 1]) * f;
+        A += __ldcg(&ap.part_acc[(pb + sp) * D + dd]) * f;
+      }
+      ap.out[(obase + h) * D + dd] = A / Ls;
+      if (dd == 0) { fin[h] = M; fin[8 + h] = Ls; }
+    }
+    if (tid == 0) ap.ticket[unit] = 0u;
+    tok_hi = n;
+  }
+  __syncthreads();
+  // ---- attention mass of every token: sum over the group of p_{h,i} ----
+  float* MS = c.mass + (static_cast<size_t>(lb) * c.Hkv + kvh) * c.slots;
+  for (int u = tok_lo + tid; u < tok_hi; u += kThreads) {
+    const int sid = (u < n8) ? u : c.cap8 + (u - n8);
+    float a = 0.0f;
+    for (int h = 0; h < g; ++h)
+      a += expf(__ldcg(&SC[static_cast<size_t>(h) * c.slots + sid]) - fin[h]) / fin[8 + h];
+    MS[sid] = a;
+  }
+}
+
+template <int D>
+cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, cudaStream_t s) {
+  const int smem = kWarps * kStages * Geo<D>::STAGE;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(k_attn_mma<D>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  k_attn_mma<D><<<dim3(c.L * c.B * c.Hkv, ap.splits), kThreads, smem, s>>>(c, ap);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStream_t s) {
+  if (c.g < 1 || c.g > 8) return cudaErrorInvalidValue;
+  if (c.d == 64) return launch_mma_d<64>(c, ap, s);
+  if (c.d == 128) return launch_mma_d<128>(c, ap, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace confkv

@@ -25,7 +25,7 @@ k_compact(Cache c, const __half* __restrict__ k_new, const __half* __restrict__ 
   const int d = c.d;
   const int nj8 = c.njobs[lb * 2], nj16 = c.njobs[lb * 2 + 1];
   const int2* j8 = c.jobs8 + static_cast<size_t>(lb) * c.cap8;
-  const int2* j16 = c.jobs16 + static_cast<size_t>(lb) * c.W;
+  const int2* j16 = c.jobs16 + static_cast<size_t>(lb) * c.Wr;
 
   // INT8 moves: 16-byte chunks of the K and V rows
   const int cpr8 = d / 16;
@@ -50,8 +50,8 @@ k_compact(Cache c, const __half* __restrict__ k_new, const __half* __restrict__ 
   }
   // FP16 moves and the new token: 16-byte chunks (8 halves)
   const int cpr16 = d / 8;
-  __half* K16 = c.k16 + static_cast<size_t>(unit) * c.W * d;
-  __half* V16 = c.v16 + static_cast<size_t>(unit) * c.W * d;
+  __half* K16 = c.k16 + static_cast<size_t>(unit) * c.Wr * d;
+  __half* V16 = c.v16 + static_cast<size_t>(unit) * c.Wr * d;
   const __half* kn = k_new + static_cast<size_t>(unit) * d;
   const __half* vn = v_new + static_cast<size_t>(unit) * d;
   for (int idx = threadIdx.x; idx < nj16 * 2 * cpr16; idx += kThreads) {
@@ -98,7 +98,7 @@ k_prefill_store(Cache c, const __half* __restrict__ k, const __half* __restrict_
         }
         if (lane == 0) (isv ? c.vs : c.ks)[static_cast<size_t>(unit) * c.cap8 + i] = s;
       } else {
-        __half* dst = (isv ? c.v16 : c.k16) + (static_cast<size_t>(unit) * c.W + (i - n8p)) * d;
+        __half* dst = (isv ? c.v16 : c.k16) + (static_cast<size_t>(unit) * c.Wr + (i - n8p)) * d;
         for (int j = lane; j < d; j += 32) dst[j] = src[j];
       }
     }
@@ -107,8 +107,8 @@ k_prefill_store(Cache c, const __half* __restrict__ k, const __half* __restrict_
         c.pos8[static_cast<size_t>(lb) * c.cap8 + i] = i;
         c.ema8[static_cast<size_t>(lb) * c.cap8 + i] = 0.0f;
       } else {
-        c.pos16[static_cast<size_t>(lb) * c.W + (i - n8p)] = i;
-        c.ema16[static_cast<size_t>(lb) * c.W + (i - n8p)] = 0.0f;
+        c.pos16[static_cast<size_t>(lb) * c.Wr + (i - n8p)] = i;
+        c.ema16[static_cast<size_t>(lb) * c.Wr + (i - n8p)] = 0.0f;
       }
     }
   }

@@ -116,9 +116,9 @@ __global__ void __launch_bounds__(kThreads) k_select(Cache c, StepParams sp) {
   const int Hkv = c.Hkv, cap8 = c.cap8, W = c.W, P = c.P;
   const size_t lbs = static_cast<size_t>(lb) * c.slots;
   int32_t* pos8 = c.pos8 + static_cast<size_t>(lb) * cap8;
-  int32_t* pos16 = c.pos16 + static_cast<size_t>(lb) * W;
+  int32_t* pos16 = c.pos16 + static_cast<size_t>(lb) * c.Wr;
   float* ema8 = c.ema8 + static_cast<size_t>(lb) * cap8;
-  float* ema16 = c.ema16 + static_cast<size_t>(lb) * W;
+  float* ema16 = c.ema16 + static_cast<size_t>(lb) * c.Wr;
   float* keys = c.keys + lbs;
   const float* mass = c.mass + static_cast<size_t>(lb) * Hkv * c.slots;
 
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) k_select(Cache c, StepParams sp) {
   {
     int toth = 0, totm = 0;
     const int lim = max(n16, n16n);
-    int2* jobs = c.jobs16 + static_cast<size_t>(lb) * W;
+    int2* jobs = c.jobs16 + static_cast<size_t>(lb) * c.Wr;
     for (int base = 0; base < lim; base += kThreads) {
       const int j = base + tid;
       const bool kn = (j < n16) && j != jage && kept(false, j);
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kThreads) k_select(Cache c, StepParams sp) {
   // ---- phase C: metadata moves (INT8 destinations first: the aging token is
   // read from its FP16 slot before any FP16 slot is overwritten) ----
   const int2* j8 = c.jobs8 + static_cast<size_t>(lb) * cap8;
-  const int2* j16 = c.jobs16 + static_cast<size_t>(lb) * W;
+  const int2* j16 = c.jobs16 + static_cast<size_t>(lb) * c.Wr;
   for (int r = tid; r < nmov8; r += kThreads) {
     const int2 jb = j8[r];
     pos8[jb.x] = pos8[jb.y];
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads) k_select(Cache c, StepParams sp) {
       const int h = row >> 1;
       const bool isv = row & 1;
       const size_t u8 = static_cast<size_t>(lb) * Hkv + h;
-      const __half* src = (isv ? c.v16 : c.k16) + (u8 * W + jage) * c.d;
+      const __half* src = (isv ? c.v16 : c.k16) + (u8 * c.Wr + jage) * c.d;
       int8_t* dst = (isv ? c.v8 : c.k8) + (u8 * cap8 + hage) * c.d;
       float* sc = (isv ? c.vs : c.ks) + u8 * cap8 + hage;
       quantize_row_warp(src, dst, sc, c.d);

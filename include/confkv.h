@@ -74,6 +74,8 @@ typedef struct confkv_opts {
   int device;        /* CUDA device ordinal; negative = the current device
                         (a NULL opts also means the current device) */
   int attn_splits;   /* split-K factor of the attention (0 = automatic) */
+  int attn_kernel;   /* 0 automatic (tensor cores when Hq/Hkv <= 8), 1 CUDA
+                        cores, 2 tensor cores (requires Hq/Hkv <= 8) */
 } confkv_opts;
 
 /* Counters read back by confkv_stats (cumulative since create unless noted). */

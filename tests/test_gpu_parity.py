@@ -133,9 +133,46 @@ def test_gqa8_d64_pyramid():
 
 
 @pytest.mark.parametrize("splits", [1, 3])
-def test_forced_split_counts(splits):
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_forced_split_counts_and_kernels(splits, kernel):
     w = small(prefill=90, steps=40, V=64)
-    _check(parity.run(w, splits=splits))
+    _check(parity.run(w, splits=splits, kernel=kernel))
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("Hq,Hkv,d", [(12, 12, 64), (40, 8, 128), (64, 8, 64), (6, 2, 128),
+                                      (7, 1, 64)])
+def test_attention_kernels_over_group_sizes(kernel, Hq, Hkv, d):
+    w = small(L=1, B=2, Hq=Hq, Hkv=Hkv, d=d, prefill=77, steps=25, N_high=40, N_low=60,
+              P=5, W=19, V=64)
+    _check(parity.run(w, kernel=kernel))
+
+
+def test_large_values_and_scale_extremes():
+    # keys/values far from N(0,1): exercises the per-chunk power-of-two scaling
+    rng = np.random.default_rng(9)
+    w = small(L=1, B=1, prefill=100, steps=20, V=64)
+
+    def big(s, lg):
+        return lg
+    import confidence_gated_kv_logits_gb300 as pkg
+    kv = pkg.ConfKV.for_workload(w, device=0)
+    orc = oracle.Oracle.for_workload(w)
+    k = (rng.standard_normal((w.Hkv, 100, w.d)) * 300).astype(np.float16)
+    v = (rng.standard_normal((w.Hkv, 100, w.d)) * np.logspace(-4, 2, 100)[None, :, None]
+         ).astype(np.float16)
+    orc.prefill_lb(0, 0, k, v)
+    kv.prefill(torch.from_numpy(k[None, None]).to(DEV), torch.from_numpy(v[None, None]).to(DEV), 100)
+    out = torch.zeros(1, 1, w.Hq, w.d, device=DEV)
+    for s in range(w.steps):
+        lg, q, kn, vn = wl.step_inputs(w, s)
+        q = (q.astype(np.float32) * 0.01).astype(np.float16)
+        kv.step(*(torch.from_numpy(np.ascontiguousarray(x)).to(DEV) for x in (lg, q, kn, vn)), out)
+        r = orc.step(lg, q, kn, vn)
+        torch.cuda.synchronize()
+        o = out.cpu().numpy()
+        assert np.max(np.abs(o - r["out"])) < 1e-3 * max(1.0, np.max(np.abs(r["out"])))
+    kv.close()
 
 
 def test_sliding_window_special_case_is_exact():
