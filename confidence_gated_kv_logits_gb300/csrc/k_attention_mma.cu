@@ -35,7 +35,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr uint32_t kBias = 0x80808080u;     // int8 -> biased uint8
 constexpr uint32_t kMagic = 0x64646464u;    // fp16 exponent byte of 1024
 constexpr uint32_t kH1152 = 0x64806480u;    // half2(1152, 1152)
@@ -119,8 +119,18 @@ __device__ __forceinline__ float gsum8(float v) {
   v += __shfl_xor_sync(0xffffffffu, v, 8);
   return v + __shfl_xor_sync(0xffffffffu, v, 16);
 }
+constexpr float kL2E = 1.4426950408889634f;
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float rescale(float m_old, float m_new) {
-  return (m_old == -INFINITY) ? 0.0f : expf(m_old - m_new);
+  return (m_old == -INFINITY) ? 0.0f : ex2((m_old - m_new) * kL2E);
+}
+// 2^e as a float for |e| <= 126 (exact)
+__device__ __forceinline__ float pow2i(int e) {
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
 // cp.async of one chunk into a stage.  INT8 chunk ci: slots 32ci..32ci+31
@@ -182,7 +192,7 @@ struct SoftState {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap) {
+__global__ void __launch_bounds__(kThreads, 3) k_attn_mma(Cache c, AttnParams ap) {
   using G = Geo<D>;
   extern __shared__ __align__(16) unsigned char smem[];
   const int unit = blockIdx.x, split = blockIdx.y;
@@ -226,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap
     mxA = gmax8(mxA);
     mxB = gmax8(mxB);
     const float nA = fmaxf(ss.mA, mxA), nB = fmaxf(ss.mB, mxB);
-    const float f = ldexpf(1.0f, Enew - ss.E);
+    const float f = pow2i(Enew - ss.E);
     const float cA = rescale(ss.mA, nA), cB = rescale(ss.mB, nB);
     ss.lA *= cA;
     ss.lB *= cB;
@@ -241,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap
     ss.mA = nA;
     ss.mB = nB;
     ss.E = Enew;
-    return ldexpf(1.0f, Enew);
+    return pow2i(Enew);
   };
   // P' (4 values of the score layout) -> hi/lo B operands, then P'.V MMAs
   auto pv_int8 = [&](const float (&x)[4], const uint32_t (&vw)[4][G::VPT / 4]) {
@@ -299,39 +309,46 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap
       cp_commit();
     }
     const int ci = cb + warp + kWarps * i;
-    const int sidx = i % kStages;
-    const uint32_t st = wbase + sidx * G::STAGE;
+    const uint32_t st = wbase + (i % kStages) * G::STAGE;
     if (ci < nc8) {
       // ------------------------- INT8 chunk: 32 tokens -------------------------
-      const float* sks = fbase + (sidx * G::STAGE + G::DATA) / 4;
-      const float* svs = sks + 32;
+      const uint32_t sks = st + G::DATA, svs = sks + 128;
       const int tb = 32 * ci;
-      float s[2][4];
-      float vmax = 0.0f;
+      uint32_t kw[2][2][G::KS];
 #pragma unroll
-      for (int sb = 0; sb < 2; ++sb) {
-        uint32_t kw[2][G::KS];
+      for (int sb = 0; sb < 2; ++sb)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
 #pragma unroll
           for (int u = 0; u < G::KPT / 16; ++u) {
             const uint4 v = lds128(tp(st, lane, (2 * sb + r) * G::KPT + 16 * u));
-            kw[r][4 * u] = v.x;
-            kw[r][4 * u + 1] = v.y;
-            kw[r][4 * u + 2] = v.z;
-            kw[r][4 * u + 3] = v.w;
+            kw[sb][r][4 * u] = v.x;
+            kw[sb][r][4 * u + 1] = v.y;
+            kw[sb][r][4 * u + 2] = v.z;
+            kw[sb][r][4 * u + 3] = v.w;
           }
-        s[sb][0] = s[sb][1] = s[sb][2] = s[sb][3] = 0.0f;
+      float s[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
-        for (int kk = 0; kk < G::KS; ++kk) {
-          const uint32_t w0 = kw[0][kk] ^ kBias, w1 = kw[1][kk] ^ kBias;
+      for (int kk = 0; kk < G::KS; ++kk) {
+#pragma unroll
+        for (int sb = 0; sb < 2; ++sb) {          // two independent accumulation chains
+          const uint32_t w0 = kw[sb][0][kk] ^ kBias, w1 = kw[sb][1][kk] ^ kBias;
           const uint32_t a[4] = {i8h2(w0, 0x4140u), i8h2(w1, 0x4140u), i8h2(w0, 0x4342u),
                                  i8h2(w1, 0x4342u)};
           mma16816(s[sb], a, qb[kk][0], qb[kk][1]);
         }
+      }
+      float vsr[2][2];
+      float vmax = 0.0f;
+#pragma unroll
+      for (int sb = 0; sb < 2; ++sb) {
         const int t0 = tb + 16 * sb + gid, t1 = t0 + 8;
         const bool v0 = t0 < n8, v1 = t1 < n8;
-        const float k0 = sks[16 * sb + gid] * ap.scale, k1 = sks[16 * sb + gid + 8] * ap.scale;
+        const float k0 = ldsf(sks + 4 * (16 * sb + gid)) * ap.scale;
+        const float k1 = ldsf(sks + 4 * (16 * sb + gid + 8)) * ap.scale;
+        vsr[sb][0] = v0 ? ldsf(svs + 4 * (16 * sb + gid)) : 0.0f;
+        vsr[sb][1] = v1 ? ldsf(svs + 4 * (16 * sb + gid + 8)) : 0.0f;
+        vmax = fmaxf(vmax, fmaxf(vsr[sb][0], vsr[sb][1]));
         s[sb][0] = v0 ? s[sb][0] * k0 : -INFINITY;
         s[sb][1] = v0 ? s[sb][1] * k0 : -INFINITY;
         s[sb][2] = v1 ? s[sb][2] * k1 : -INFINITY;
@@ -344,26 +361,23 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap
           if (v0) SC[static_cast<size_t>(2 * t4 + 1) * c.slots + t0] = s[sb][1];
           if (v1) SC[static_cast<size_t>(2 * t4 + 1) * c.slots + t1] = s[sb][3];
         }
-        if (v0) vmax = fmaxf(vmax, svs[16 * sb + gid]);
-        if (v1) vmax = fmaxf(vmax, svs[16 * sb + gid + 8]);
       }
       vmax = gmax8(vmax);
       vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
       vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
-      int e = 0;
-      frexpf(vmax, &e);
+      // vmax = f * 2^e, f in [0.5, 1): P' * 2^(14 - e) < 2^14
+      const int e = static_cast<int>((__float_as_uint(vmax) >> 23) & 0xffu) - 126;
       const int Enew = (vmax > 0.0f) ? max(-60, min(60, 14 - e)) : ss.E;
       const float two = update(fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2])),
                                fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3])), Enew);
+      const float mLA = ss.mA * kL2E, mLB = ss.mB * kL2E;
 #pragma unroll
       for (int sb = 0; sb < 2; ++sb) {
-        const float pA0 = expf(s[sb][0] - ss.mA), pB0 = expf(s[sb][1] - ss.mB);
-        const float pA1 = expf(s[sb][2] - ss.mA), pB1 = expf(s[sb][3] - ss.mB);
+        const float pA0 = ex2(fmaf(s[sb][0], kL2E, -mLA)), pB0 = ex2(fmaf(s[sb][1], kL2E, -mLB));
+        const float pA1 = ex2(fmaf(s[sb][2], kL2E, -mLA)), pB1 = ex2(fmaf(s[sb][3], kL2E, -mLB));
         ss.lA += pA0 + pA1;
         ss.lB += pB0 + pB1;
-        const int t0 = tb + 16 * sb + gid;
-        const float vs0 = (t0 < n8) ? svs[16 * sb + gid] * two : 0.0f;
-        const float vs1 = (t0 + 8 < n8) ? svs[16 * sb + gid + 8] * two : 0.0f;
+        const float vs0 = vsr[sb][0] * two, vs1 = vsr[sb][1] * two;
         const float x[4] = {pA0 * vs0, pB0 * vs0, pA1 * vs1, pB1 * vs1};
         uint32_t vw[4][G::VPT / 4];
 #pragma unroll
@@ -398,11 +412,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap
           kw[r][4 * u + 3] = v.w;
         }
       float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      float s2[4] = {0.0f, 0.0f, 0.0f, 0.0f};      // second chain: odd k-steps
 #pragma unroll
-      for (int kk = 0; kk < G::KS; ++kk) {
+      for (int kk = 0; kk < G::KS; kk += 2) {
         const uint32_t a[4] = {kw[0][2 * kk], kw[1][2 * kk], kw[0][2 * kk + 1], kw[1][2 * kk + 1]};
         mma16816(s, a, qb[kk][0], qb[kk][1]);
+        const uint32_t a2[4] = {kw[0][2 * kk + 2], kw[1][2 * kk + 2], kw[0][2 * kk + 3],
+                                kw[1][2 * kk + 3]};
+        mma16816(s2, a2, qb[kk + 1][0], qb[kk + 1][1]);
       }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[j] += s2[j];
       const int t0 = tb + gid, t1 = t0 + 8;
       const bool v0 = t0 < n16, v1 = t1 < n16;
       s[0] = v0 ? s[0] * ap.scale : -INFINITY;
@@ -419,8 +439,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap
         if (v1) SC[static_cast<size_t>(2 * t4 + 1) * c.slots + o1] = s[3];
       }
       const float two = update(fmaxf(s[0], s[2]), fmaxf(s[1], s[3]), 13);
-      const float pA0 = expf(s[0] - ss.mA), pB0 = expf(s[1] - ss.mB);
-      const float pA1 = expf(s[2] - ss.mA), pB1 = expf(s[3] - ss.mB);
+      const float mLA = ss.mA * kL2E, mLB = ss.mB * kL2E;
+      const float pA0 = ex2(fmaf(s[0], kL2E, -mLA)), pB0 = ex2(fmaf(s[1], kL2E, -mLB));
+      const float pA1 = ex2(fmaf(s[2], kL2E, -mLA)), pB1 = ex2(fmaf(s[3], kL2E, -mLB));
       ss.lA += pA0 + pA1;
       ss.lB += pB0 + pB1;
       const float x[4] = {pA0 * two, pB0 * two, pA1 * two, pB1 * two};
@@ -436,10 +457,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap
           vw[ii][4 * u + 3] = v.w;
         }
       // zero the V rows of tokens past the region end (stale slots)
-      if (!(2 * t4 < n16 - tb)) { for (int u = 0; u < G::VPT / 2; ++u) vw[0][u] = 0u; }
-      if (!(2 * t4 + 1 < n16 - tb)) { for (int u = 0; u < G::VPT / 2; ++u) vw[1][u] = 0u; }
-      if (!(2 * t4 + 8 < n16 - tb)) { for (int u = 0; u < G::VPT / 2; ++u) vw[2][u] = 0u; }
-      if (!(2 * t4 + 9 < n16 - tb)) { for (int u = 0; u < G::VPT / 2; ++u) vw[3][u] = 0u; }
+      const int rem = n16 - tb;
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+        if (!(2 * t4 + (ii & 1) + 8 * (ii >> 1) < rem))
+#pragma unroll
+          for (int u = 0; u < G::VPT / 2; ++u) vw[ii][u] = 0u;
       pv_f16(x, vw);
     }
   }
@@ -453,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap
   float* wl = wm + kWarps * 8;                           // [kWarps][8]
   float* fin = wl + kWarps * 8;                          // [2][8]
   float* wo = fin + 16;                                  // [kWarps][8][D]
-  const float unscale = ldexpf(1.0f, -ss.E);
+  const float unscale = pow2i(-ss.E);
   if (gid == 0) {
     wm[warp * 8 + 2 * t4] = ss.mA;
     wm[warp * 8 + 2 * t4 + 1] = ss.mB;
@@ -491,10 +514,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap
       if (dd == 0) { ap.part_ml[pi * 2] = M; ap.part_ml[pi * 2 + 1] = Ls; }
     }
   }
-  int tok_lo = 0, tok_hi = 0;   // unified token range whose mass this CTA writes
-  if (ap.splits == 1) {
-    tok_hi = n;
-  } else {
+  if (ap.splits > 1) {
     __shared__ int s_last;
     __threadfence();
     __syncthreads();
@@ -517,17 +537,39 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_mma(Cache c, AttnParams ap
       if (dd == 0) { fin[h] = M; fin[8 + h] = Ls; }
     }
     if (tid == 0) ap.ticket[unit] = 0u;
-    tok_hi = n;
   }
   __syncthreads();
   // ---- attention mass of every token: sum over the group of p_{h,i} ----
+  // Both regions start 16-byte aligned (cap8 % 32 == 0, slots % 16 == 0), so
+  // four consecutive tokens of every head are read with one 128-bit load.
+  float ML[8], iL[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    ML[h] = (h < g) ? fin[h] * kL2E : 0.0f;
+    iL[h] = (h < g) ? 1.0f / fin[8 + h] : 0.0f;
+  }
   float* MS = c.mass + (static_cast<size_t>(lb) * c.Hkv + kvh) * c.slots;
-  for (int u = tok_lo + tid; u < tok_hi; u += kThreads) {
-    const int sid = (u < n8) ? u : c.cap8 + (u - n8);
-    float a = 0.0f;
-    for (int h = 0; h < g; ++h)
-      a += expf(__ldcg(&SC[static_cast<size_t>(h) * c.slots + sid]) - fin[h]) / fin[8 + h];
-    MS[sid] = a;
+  for (int region = 0; region < 2; ++region) {
+    const int cnt_r = region ? n16 : n8;
+    const int base = region ? c.cap8 : 0;
+    for (int j = tid; 4 * j < cnt_r; j += kThreads) {
+      float4 sv[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        if (h < g)
+          sv[h] = __ldcg(reinterpret_cast<const float4*>(SC + static_cast<size_t>(h) * c.slots + base) + j);
+      float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        if (h < g) {
+          a.x += ex2(fmaf(sv[h].x, kL2E, -ML[h])) * iL[h];
+          a.y += ex2(fmaf(sv[h].y, kL2E, -ML[h])) * iL[h];
+          a.z += ex2(fmaf(sv[h].z, kL2E, -ML[h])) * iL[h];
+          a.w += ex2(fmaf(sv[h].w, kL2E, -ML[h])) * iL[h];
+        }
+      // slots past the region end hold stale scores; their mass is never read
+      reinterpret_cast<float4*>(MS + base)[j] = a;
+    }
   }
 }
 
