@@ -365,6 +365,17 @@ def run_ours(args):
     prof = kv.profile_read()
     kv.profile(())
     st1, rc = kv.stats()
+    # per-kernel breakdown: a separate pass of further decode steps with every
+    # kernel bracketed by events (kept out of the timed region above)
+    breakdown = {}
+    nb = min(32, K)
+    kv.profile(list(kv.KERNELS))
+    for s in range(nb):
+        kv.step(LG[Wm + s], Q[Wm + s], KN[Wm + s], VN[Wm + s], out, kp, kc, cf, bd)
+    for name, (n_l, tot) in kv.profile_read().items():
+        if n_l:
+            breakdown[name] = {"launches": n_l, "avg_us": 1e3 * tot / n_l}
+    kv.profile(())
     ms_max = allmax(ms, ws)
     value = ws * w.B * K / (ms_max / 1e3)
     attn_launches, attn_ms = prof["attention"]
@@ -445,6 +456,7 @@ def run_ours(args):
                          "achieved_gbs": pipe, "frac": pipe / hbm,
                          "attention_share_of_step": attn_ms / ms},
             "budget_high_fraction": hi_frac,
+            "kernels_us": breakdown,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": 4 * K,

@@ -24,7 +24,9 @@ namespace {
 
 constexpr int kSmCount = 152;
 constexpr int kProfKernels = 4;
-const char* const kProfNames[kProfKernels] = {"confidence", "select", "compact", "attention"};
+// "select" covers ranking, eviction, compaction moves and INT8 aging; slot 2
+// is unused (kept so that the kernel mask bits stay stable).
+const char* const kProfNames[kProfKernels] = {"confidence", "select", "unused", "attention"};
 
 struct DeviceGuard {
   int prev = -1;
@@ -49,6 +51,8 @@ struct confkv_ctx {
   Cache cache{};
   float* conf = nullptr;
   int32_t* hi = nullptr;
+  confkv::ConfPart* conf_part = nullptr;
+  unsigned int* conf_ticket = nullptr;
   int32_t* btab = nullptr;
   float* part_ml = nullptr;
   float* part_acc = nullptr;
@@ -226,13 +230,12 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   A(dalloc(c, &k.keys, LB * c->slots));
   A(dalloc(c, &k.n8, LB));
   A(dalloc(c, &k.n16, LB));
-  A(dalloc(c, &k.jobs8, LB * c->cap8));
-  A(dalloc(c, &k.jobs16, LB * c->Wr));
-  A(dalloc(c, &k.njobs, LB * 2));
   A(dalloc(c, &k.stats, 1));
   A(dalloc(c, &k.err, 1));
   A(dalloc(c, &c->conf, c->B));
   A(dalloc(c, &c->hi, c->B));
+  A(dalloc(c, &c->conf_part, static_cast<size_t>(c->B) * confkv::confidence_ctas_per_seq(c->B, c->V)));
+  A(dalloc(c, &c->conf_ticket, c->B));
   A(dalloc(c, &c->btab, static_cast<size_t>(c->L) * 2));
   A(dalloc(c, &c->part_ml, LB * c->Hq * c->splits * 2));
   A(dalloc(c, &c->part_acc, LB * c->Hq * c->splits * c->d));
@@ -296,7 +299,8 @@ int confkv_step(confkv_ctx* c, const float* logits, const uint16_t* q, const uin
   cudaError_t e;
   prof_mark(c, 0, s);
   e = confkv::launch_confidence(logits, c->B, c->V, c->tau, c->N_low, c->N_high, c->conf, c->hi,
-                                conf_out, budget_out, c->cache.err, c->cache.stats, s);
+                                conf_out, budget_out, c->cache.err, c->cache.stats,
+                                c->conf_part, c->conf_ticket, s);
   prof_mark(c, 0, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("confidence: ") + cudaGetErrorString(e));
   StepParams sp{};
@@ -307,15 +311,12 @@ int confkv_step(confkv_ctx* c, const float* logits, const uint16_t* q, const uin
   sp.hi = c->hi;
   sp.kept_pos = kept_pos;
   sp.kept_count = kept_count;
+  sp.k_new = reinterpret_cast<const __half*>(k_new);
+  sp.v_new = reinterpret_cast<const __half*>(v_new);
   prof_mark(c, 1, s);
   e = confkv::launch_select(c->cache, sp, s);
   prof_mark(c, 1, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("select: ") + cudaGetErrorString(e));
-  prof_mark(c, 2, s);
-  e = confkv::launch_compact(c->cache, reinterpret_cast<const __half*>(k_new),
-                             reinterpret_cast<const __half*>(v_new), s);
-  prof_mark(c, 2, s);
-  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("compact: ") + cudaGetErrorString(e));
   prof_mark(c, 3, s);
   const int rc = run_attention(c, reinterpret_cast<const __half*>(q), out, s);
   prof_mark(c, 3, s);

@@ -31,6 +31,11 @@ struct DevStats {
   unsigned long long hi_steps;
 };
 
+struct ConfPart {       // partial confidence state of one CTA
+  float m1, m2, S, T;
+  int bad;
+};
+
 struct Cache {
   int L, B, Hq, Hkv, d, g, W, Wr, P, cap8, slots, Ncap;
   int8_t* k8;
@@ -48,9 +53,6 @@ struct Cache {
   float* keys;      // [L*B][slots] ranking keys of the current step
   int32_t* n8;
   int32_t* n16;
-  int2* jobs8;      // [L*B][cap8]  (dst INT8 slot, src INT8 slot)
-  int2* jobs16;     // [L*B][Wr]     (dst FP16 slot, src FP16 slot or -1 = new token)
-  int32_t* njobs;   // [L*B][2]     INT8 moves, FP16 writes
   DevStats* stats;
   int32_t* err;
 };
@@ -62,6 +64,8 @@ struct StepParams {
   const int32_t* hi;     // [B] 1 if the sequence chose N_high
   int32_t* kept_pos;     // [L*B][Ncap] or null
   int32_t* kept_count;   // [L*B] or null
+  const __half* k_new;   // [L*B][Hkv][d] key / value of the new token
+  const __half* v_new;
 };
 
 struct AttnParams {
@@ -76,13 +80,12 @@ struct AttnParams {
 };
 
 // ---- launch wrappers (each file owns its kernels) ----
+int confidence_ctas_per_seq(int B, int V);
 cudaError_t launch_confidence(const float* logits, int B, int V, float tau, int N_low,
                               int N_high, float* conf, int32_t* hi, float* conf_out,
-                              int32_t* budget_out, int32_t* err, DevStats* st,
-                              cudaStream_t s);
+                              int32_t* budget_out, int32_t* err, DevStats* st, ConfPart* part,
+                              unsigned int* ticket, cudaStream_t s);
 cudaError_t launch_select(const Cache& c, const StepParams& sp, cudaStream_t s);
-cudaError_t launch_compact(const Cache& c, const __half* k_new, const __half* v_new,
-                           cudaStream_t s);
 cudaError_t launch_prefill_store(const Cache& c, const __half* k, const __half* v, int T,
                                  cudaStream_t s);
 cudaError_t launch_attention(const Cache& c, const AttnParams& ap, cudaStream_t s);

@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_attn_mma(Cache c, AttnParams ap
   extern __shared__ __align__(16) unsigned char smem[];
   const int unit = blockIdx.x, split = blockIdx.y;
   const int lb = unit / c.Hkv, kvh = unit - lb * c.Hkv, g = c.g;
-  const int n8 = c.n8[lb], n16 = c.n16[lb], n = n8 + n16;
+  const int n8 = c.n8[lb], n16 = c.n16[lb];
   const int nc8 = (n8 + 31) >> 5, nc16 = (n16 + 15) >> 4, nc = nc8 + nc16;
   const int cb = static_cast<int>(static_cast<long long>(nc) * split / ap.splits);
   const int ce = static_cast<int>(static_cast<long long>(nc) * (split + 1) / ap.splits);

@@ -7,15 +7,15 @@
 //                         top tokens and p(1) the top probability;
 //   Adaptieve Budgetselectie  c >= tau -> N_high, else N_low.
 //
-// One thread-block cluster of kClusterCtas CTAs per sequence streams its V
-// logits once with 128-bit loads (each CTA one contiguous chunk).  Each thread
-// keeps an online state (top-1, top-2, S = sum e^(z-top1),
-// T = sum e^(z-top1)(z-top1)); states are merged by warp shuffles, shared
-// memory and, across the cluster, distributed shared memory read by CTA rank
-// 0 after a hardware cluster barrier.  With p_i = e^(z_i - z*)/S:
+// Each sequence's V logits are split over enough CTAs to cover every SM
+// (each thread kBatch coalesced loads in flight).  Each thread reduces its
+// registers to a state (top-1, top-2, S = sum e^(z-top1),
+// T = sum e^(z-top1)(z-top1)); states are merged by warp shuffles and shared
+// memory, stored per CTA, and the CTA that takes the last ticket of its
+// sequence (an atomic counter; no CTA waits) merges them and picks the
+// budget.  The sums are fp32 (exponentials by ex2.approx: ~1e-7 relative),
+// well inside the 1e-5 tolerance on c.  With p_i = e^(z_i - z*)/S:
 //   H = ln S - T/S,  p(1) = 1/S,  m = z(1) - z(2).
-#include <cooperative_groups.h>
-
 #include <cfloat>
 
 #include "confkv_internal.cuh"
@@ -28,26 +28,11 @@ struct ConfState {
   int bad;
 };
 
-__device__ __forceinline__ void add_elem(ConfState& st, float x) {
-  if (isnan(x) || x == INFINITY) { st.bad = 1; return; }
-  if (x == -INFINITY) return;                       // masked token
-  if (x > st.m1) {
-    if (st.S > 0.0f) {
-      const float dlt = st.m1 - x;                  // < 0
-      const float f = expf(dlt);
-      st.T = f * (st.T + dlt * st.S);
-      st.S = f * st.S;
-    }
-    st.m2 = st.m1;
-    st.m1 = x;
-    st.S += 1.0f;
-  } else {
-    if (x > st.m2) st.m2 = x;
-    const float dlt = x - st.m1;
-    const float e = expf(dlt);
-    st.S += e;
-    st.T = fmaf(e, dlt, st.T);
-  }
+constexpr float kL2E = 1.4426950408889634f;
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ ConfState merge(const ConfState& a, const ConfState& b) {
@@ -59,13 +44,13 @@ __device__ __forceinline__ ConfState merge(const ConfState& a, const ConfState& 
   r.T = 0.0f;
   if (a.S > 0.0f) {
     const float dlt = a.m1 - r.m1;
-    const float f = expf(dlt);
+    const float f = ex2(dlt * kL2E);
     r.S += f * a.S;
     r.T += f * (a.T + dlt * a.S);
   }
   if (b.S > 0.0f) {
     const float dlt = b.m1 - r.m1;
-    const float f = expf(dlt);
+    const float f = ex2(dlt * kL2E);
     r.S += f * b.S;
     r.T += f * (b.T + dlt * b.S);
   }
@@ -82,45 +67,53 @@ __device__ __forceinline__ ConfState shfl_xor(const ConfState& s, int o) {
   return r;
 }
 
-constexpr int kThreads = 1024;
-constexpr int kClusterCtas = 8;
+constexpr int kThreads = 512;
+constexpr int kBatch = 8;      // logits per thread in flight per batch
 
-__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads)
-k_confidence(const float* __restrict__ logits, int V, float tau, int N_low, int N_high,
+__global__ void __launch_bounds__(kThreads)
+k_confidence(const float* __restrict__ logits, int V, int cps, float tau, int N_low, int N_high,
              float* conf, int32_t* hi, float* conf_out, int32_t* budget_out, int32_t* err,
-             DevStats* st) {
-  namespace cg = cooperative_groups;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int b = blockIdx.x / kClusterCtas;
-  const int rank = static_cast<int>(cluster.block_rank());
-  // chunk of this CTA: multiples of 4 elements so that the 128-bit body stays aligned
-  const int per = ((V + kClusterCtas - 1) / kClusterCtas + 3) & ~3;
-  const int lo = min(V, rank * per), hi_ = min(V, lo + per);
+             DevStats* st, ConfPart* part, unsigned int* ticket) {
+  const int b = blockIdx.x / cps;
+  const int rk = blockIdx.x - b * cps;
+  const long long lo = static_cast<long long>(V) * rk / cps;
+  const long long hi_ = static_cast<long long>(V) * (rk + 1) / cps;
   const float* z = logits + static_cast<size_t>(b) * V + lo;
-  const int Vc = hi_ - lo;
+  const int Vc = static_cast<int>(hi_ - lo);
   ConfState s{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
-
-  // 128-bit loads over the 16-byte aligned body, scalar head and tail.
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(z);
-  int head = static_cast<int>(((16 - (addr & 15)) & 15) / 4);
-  if (head > Vc) head = Vc;
-  for (int i = threadIdx.x; i < head; i += kThreads) add_elem(s, z[i]);
-  const int nvec = (Vc - head) / 4;
-  const float4* zv = reinterpret_cast<const float4*>(z + head);
-  for (int i = threadIdx.x; i < nvec; i += kThreads) {
-    const float4 x = __ldcs(zv + i);
-    add_elem(s, x.x);
-    add_elem(s, x.y);
-    add_elem(s, x.z);
-    add_elem(s, x.w);
+  for (int base = 0; base < Vc; base += kBatch * kThreads) {
+    float x[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int i = base + k * kThreads + threadIdx.x;
+      x[k] = (i < Vc) ? __ldcs(z + i) : -INFINITY;      // -inf: outside the chunk
+    }
+    // top-1 / top-2 (ties count twice) and the NaN / +inf test, branch-free
+    ConfState bs{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
+    int bad = 0;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      bad |= !(x[k] < INFINITY) && !(x[k] == -INFINITY);
+      bs.m2 = fmaxf(bs.m2, fminf(bs.m1, x[k]));
+      bs.m1 = fmaxf(bs.m1, x[k]);
+    }
+    bs.bad = bad;
+    if (bs.m1 > -INFINITY) {
+      const float ml = bs.m1 * kL2E;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const float xc = fmaxf(x[k], -3.0e38f);            // masked tokens -> weight 0
+        const float e = ex2(fmaf(xc, kL2E, -ml));
+        bs.S += e;
+        bs.T = fmaf(e, xc - bs.m1, bs.T);
+      }
+    }
+    s = merge(s, bs);
   }
-  for (int i = head + nvec * 4 + threadIdx.x; i < Vc; i += kThreads) add_elem(s, z[i]);
-
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s = merge(s, shfl_xor(s, o));
-
   __shared__ ConfState sh[kThreads / 32];
-  __shared__ ConfState cta_state;
+  __shared__ int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) sh[warp] = s;
   __syncthreads();
@@ -128,48 +121,62 @@ k_confidence(const float* __restrict__ logits, int V, float tau, int N_low, int 
     s = (lane < kThreads / 32) ? sh[lane] : ConfState{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s = merge(s, shfl_xor(s, o));
-    if (lane == 0) cta_state = s;
-  }
-  cluster.sync();                        // every CTA's state is visible cluster-wide
-  if (rank == 0 && warp == 0) {
-    s = (lane < kClusterCtas) ? *cluster.map_shared_rank(&cta_state, lane)
-                              : ConfState{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s = merge(s, shfl_xor(s, o));
     if (lane == 0) {
-      double c = 0.0;
-      const bool bad = s.bad || !(s.S > 0.0f);
-      if (!bad) {
-        const double S = s.S, T = s.T;
-        const double H = log(S) - T / S;
-        const double Hn = H / log(static_cast<double>(V));
-        const double m = static_cast<double>(s.m1) - static_cast<double>(s.m2);
-        const double sig = 1.0 / (1.0 + exp(-m));
-        c = 0.4 * (1.0 - Hn) + 0.3 * sig + 0.3 / S;
-      } else {
-        atomicOr(err, 1);
-      }
-      const float cf = static_cast<float>(c);
-      const int h = (!bad && cf >= tau) ? 1 : 0;
-      conf[b] = cf;
-      hi[b] = h;
-      if (conf_out) conf_out[b] = cf;
-      if (budget_out) budget_out[b] = h ? N_high : N_low;
-      atomicAdd(&st->logits_bytes, static_cast<unsigned long long>(V) * 4ull);
-      if (h) atomicAdd(&st->hi_steps, 1ull);
+      part[blockIdx.x] = ConfPart{s.m1, s.m2, s.S, s.T, s.bad};
+      __threadfence();
+      s_last = (atomicAdd(&ticket[b], 1u) == static_cast<unsigned>(cps - 1));
     }
   }
-  cluster.sync();                        // keep remote shared memory alive until read
+  __syncthreads();
+  if (!s_last || warp != 0) return;
+  // last CTA of sequence b: merge every CTA's state (no CTA waits)
+  __threadfence();
+  s = ConfState{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
+  for (int i = lane; i < cps; i += 32) {
+    const ConfPart* pp = part + static_cast<size_t>(b) * cps + i;
+    ConfState q{__ldcg(&pp->m1), __ldcg(&pp->m2), __ldcg(&pp->S), __ldcg(&pp->T), __ldcg(&pp->bad)};
+    s = merge(s, q);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s = merge(s, shfl_xor(s, o));
+  if (lane == 0) {
+    ticket[b] = 0u;
+    float c = 0.0f;
+    const bool bad = s.bad || !(s.S > 0.0f);
+    if (!bad) {
+      const float H = logf(s.S) - s.T / s.S;
+      const float Hn = H / logf(static_cast<float>(V));
+      const float m = s.m1 - s.m2;                      // +inf when one finite logit
+      const float sig = 1.0f / (1.0f + expf(-m));
+      c = 0.4f * (1.0f - Hn) + 0.3f * sig + 0.3f / s.S;
+    } else {
+      atomicOr(err, 1);
+    }
+    const int h = (!bad && c >= tau) ? 1 : 0;
+    conf[b] = c;
+    hi[b] = h;
+    if (conf_out) conf_out[b] = c;
+    if (budget_out) budget_out[b] = h ? N_high : N_low;
+    atomicAdd(&st->logits_bytes, static_cast<unsigned long long>(V) * 4ull);
+    if (h) atomicAdd(&st->hi_steps, 1ull);
+  }
 }
 
 }  // namespace
 
+int confidence_ctas_per_seq(int B, int V) {
+  const int want = (2 * 152 + B - 1) / B;                  // fill the GPU twice
+  const int by_size = (V + kThreads * 2 - 1) / (kThreads * 2);
+  return max(1, min(want, by_size));
+}
+
 cudaError_t launch_confidence(const float* logits, int B, int V, float tau, int N_low,
                               int N_high, float* conf, int32_t* hi, float* conf_out,
-                              int32_t* budget_out, int32_t* err, DevStats* st,
-                              cudaStream_t s) {
-  k_confidence<<<B * kClusterCtas, kThreads, 0, s>>>(logits, V, tau, N_low, N_high, conf, hi, conf_out,
-                                      budget_out, err, st);
+                              int32_t* budget_out, int32_t* err, DevStats* st, ConfPart* part,
+                              unsigned int* ticket, cudaStream_t s) {
+  const int cps = confidence_ctas_per_seq(B, V);
+  k_confidence<<<B * cps, kThreads, 0, s>>>(logits, V, cps, tau, N_low, N_high, conf, hi,
+                                            conf_out, budget_out, err, st, part, ticket);
   return cudaGetLastError();
 }
 

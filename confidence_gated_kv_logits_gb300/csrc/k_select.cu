@@ -19,7 +19,9 @@
 // The fp32 operations use explicit _rn intrinsics so that no contraction
 // changes the rounding: the decision is taken in fp32 on exact fp32 values.
 //
-// One CTA of kThreads per (layer, sequence).  Selection: the need-th largest
+// One CTA of kThreads per (layer, sequence).  The same CTA then applies the
+// compaction: metadata and K/V data moves of every KV head, the INT8
+// quantisation of the aging token and the write of the new token.  Selection: the need-th largest
 // 64-bit key (key bits << 32 | position; unique) is found by an 8-bit MSB
 // radix select over the candidates (early exit once the boundary bucket is
 // taken whole); a single eviction, the steady state, is one arg-min.
@@ -32,40 +34,74 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kReg = 4;        // slots per thread held in registers
 
 __device__ __forceinline__ unsigned long long key64(float key, int pos) {
   return (static_cast<unsigned long long>(__float_as_uint(key)) << 32) |
          static_cast<unsigned int>(pos);
 }
 
-// Block-wide exclusive scan of two flags; returns the ranks, accumulates totals.
-struct Scan2 {
-  int* wsum;  // smem [2][kWarps]
-};
-
-__device__ __forceinline__ void block_scan2(bool fa, bool fb, int* wsum, int& ra, int& rb,
-                                            int& tota, int& totb) {
+// Block-wide exclusive scan of two per-thread counts (ranks in thread order).
+__device__ __forceinline__ void block_scan2(int& a, int& b, int* wsum, int& tot_a, int& tot_b) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned ba = __ballot_sync(0xffffffffu, fa);
-  const unsigned bb = __ballot_sync(0xffffffffu, fb);
-  const unsigned lt = (1u << lane) - 1u;
-  if (lane == 0) {
-    wsum[warp] = __popc(ba);
-    wsum[kWarps + warp] = __popc(bb);
+  int ia = a, ib = b;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int xa = __shfl_up_sync(0xffffffffu, ia, o);
+    const int xb = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) { ia += xa; ib += xb; }
+  }
+  if (lane == 31) {
+    wsum[warp] = ia;
+    wsum[kWarps + warp] = ib;
   }
   __syncthreads();
-  int offa = 0, offb = 0, sa = 0, sb = 0;
+  int oa = 0, ob = 0, ta = 0, tb = 0;
   for (int w = 0; w < kWarps; ++w) {
     const int xa = wsum[w], xb = wsum[kWarps + w];
-    if (w < warp) { offa += xa; offb += xb; }
-    sa += xa;
-    sb += xb;
+    if (w < warp) { oa += xa; ob += xb; }
+    ta += xa;
+    tb += xb;
   }
-  ra = tota + offa + __popc(ba & lt);
-  rb = totb + offb + __popc(bb & lt);
-  tota += sa;
-  totb += sb;
+  a = oa + ia - a;
+  b = ob + ib - b;
+  tot_a = ta;
+  tot_b = tb;
   __syncthreads();
+}
+
+// Plan of one dense region of n live slots that keeps nn of them: the slots
+// below nn that are not kept (holes) are filled, in rank order, by the kept
+// slots at or above nn (movers).  jobs[r].x = hole r, jobs[r].y = mover r.
+// Each thread scans 8 consecutive slots per pass.  Returns the mover count.
+__device__ int plan_region(const unsigned char* f, int n, int nn, int2* jobs, int* wsum) {
+  constexpr int kPer = 8;
+  const int lim = max(n, nn);
+  int hbase = 0, mbase = 0;
+  for (int base = 0; base < lim; base += kThreads * kPer) {
+    const int j0 = base + threadIdx.x * kPer;
+    int hc = 0, mc = 0;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int j = j0 + e;
+      if (j < nn) hc += (j >= n || !f[j]) ? 1 : 0;
+      else if (j < n) mc += f[j] ? 1 : 0;
+    }
+    int th, tm;
+    block_scan2(hc, mc, wsum, th, tm);
+    int rh = hbase + hc, rm = mbase + mc;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int j = j0 + e;
+      if (j < nn) {
+        if (j >= n || !f[j]) jobs[rh++].x = j;
+      } else if (j < n && f[j]) {
+        jobs[rm++].y = j;
+      }
+    }
+    hbase += th;
+    mbase += tm;
+  }
+  return mbase;
 }
 
 __device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v,
@@ -106,7 +142,7 @@ __device__ void quantize_row_warp(const __half* src, int8_t* dst, float* scale_o
   if (lane == 0) *scale_out = s;
 }
 
-__global__ void __launch_bounds__(kThreads) k_select(Cache c, StepParams sp) {
+__global__ void __launch_bounds__(kThreads, 2) k_select(Cache c, StepParams sp) {
   const int lb = blockIdx.x;
   const int l = lb / c.B, b = lb % c.B;
   const int tid = threadIdx.x;
@@ -129,49 +165,91 @@ __global__ void __launch_bounds__(kThreads) k_select(Cache c, StepParams sp) {
   if (tid == 0) { s_prot = 0; s_jage = -1; }
   __syncthreads();
 
-  // ---- phase A: EMA update and ranking keys of every cached token ----
+  // ---- phase A: EMA update and ranking keys of every cached token.
+  // Slots are taken kReg per thread per round with all loads issued first;
+  // when n <= kReg * kThreads the 64-bit keys stay in registers for the
+  // selection and the flag pass (otherwise they are re-read from `keys`).
+  const int ntok = n8 + n16;
+  const bool in_regs = ntok <= kReg * kThreads;
+  unsigned long long rkey[kReg];
+  bool rcand[kReg];
+  unsigned long long lmin = ~0ull;
+  int lprot = 0;
   const float hqf = static_cast<float>(c.Hq);
-  for (int i = tid; i < n8 + n16; i += kThreads) {
-    const bool is8 = i < n8;
-    const int j = is8 ? i : i - n8;
-    const int sid = is8 ? j : cap8 + j;
-    float asum = 0.0f;
-    for (int h = 0; h < Hkv; ++h) asum = __fadd_rn(asum, mass[static_cast<size_t>(h) * c.slots + sid]);
-    const float a = __fdiv_rn(asum, hqf);
-    float* ep = is8 ? ema8 + j : ema16 + j;
-    const float e = __fadd_rn(__fmul_rn(sp.beta, *ep), __fmul_rn(sp.omb, a));
-    *ep = e;
-    const int age = t - (is8 ? pos8[j] : pos16[j]);
-    keys[sid] = __fadd_rn(e, __fdiv_rn(1.0f, static_cast<float>(1 + age)));
-    if (!is8) {
-      if (age < P) atomicAdd(&s_prot, 1);
-      if (age == W) s_jage = j;
+  for (int base = 0; base < ntok; base += kReg * kThreads) {
+    int sid[kReg], pv[kReg];
+    float ev[kReg], asum[kReg];
+#pragma unroll
+    for (int r = 0; r < kReg; ++r) {
+      const int i = base + r * kThreads + tid;
+      const bool is8 = i < n8;
+      const int j = is8 ? i : i - n8;
+      sid[r] = (i < ntok) ? (is8 ? j : cap8 + j) : -1;
+      pv[r] = (i < ntok) ? (is8 ? pos8[j] : pos16[j]) : 0;
+      ev[r] = (i < ntok) ? (is8 ? ema8[j] : ema16[j]) : 0.0f;
+      asum[r] = 0.0f;
+    }
+    for (int h = 0; h < Hkv; ++h) {
+      const float* mh = mass + static_cast<size_t>(h) * c.slots;
+#pragma unroll
+      for (int r = 0; r < kReg; ++r)
+        if (sid[r] >= 0) asum[r] = __fadd_rn(asum[r], mh[sid[r]]);
+    }
+#pragma unroll
+    for (int r = 0; r < kReg; ++r) {
+      rcand[r] = false;
+      if (sid[r] < 0) continue;
+      const int i = base + r * kThreads + tid;
+      const bool is8 = i < n8;
+      const int j = is8 ? i : i - n8;
+      const float a = __fdiv_rn(asum[r], hqf);
+      const float e = __fadd_rn(__fmul_rn(sp.beta, ev[r]), __fmul_rn(sp.omb, a));
+      if (is8) ema8[j] = e; else ema16[j] = e;
+      const int age = t - pv[r];
+      const float key = __fadd_rn(e, __fdiv_rn(1.0f, static_cast<float>(1 + age)));
+      keys[sid[r]] = key;
+      const bool prot = !is8 && age < P;
+      if (prot) ++lprot;
+      if (!is8 && age == W) s_jage = j;
+      const unsigned long long k64 = key64(key, pv[r]);
+      rkey[r] = k64;
+      rcand[r] = !prot;
+      if (!prot) lmin = k64 < lmin ? k64 : lmin;
     }
   }
+  for (int o = 16; o > 0; o >>= 1) lprot += __shfl_xor_sync(0xffffffffu, lprot, o);
+  if ((tid & 31) == 0 && lprot) atomicAdd(&s_prot, lprot);
   __syncthreads();
   const int pcount = s_prot + 1;            // + the new token
   const int jage = s_jage;
   const int n_tot = n8 + n16 + 1;
-  // candidate test: INT8 slots always, FP16 slots when age >= P
-  // keep rule: mode 0 keep all, 1 keep none, 2 (k & mask) >= prefix, 3 k != kmin
+  // keep rule for candidates: mode 0 keep all, 1 keep none,
+  // 2 (key & mask) >= prefix, 3 key != kmin (exactly one eviction)
   int mode = 0;
   unsigned long long mask = 0, prefix = 0, kmin = 0;
+  // candidate key of slot i (unified order), or false if protected
+  auto cand_key = [&](int i, unsigned long long& k64) -> bool {
+    const bool is8 = i < n8;
+    const int j = is8 ? i : i - n8;
+    const int p = is8 ? pos8[j] : pos16[j];
+    if (!is8 && t - p < P) return false;
+    k64 = key64(keys[is8 ? j : cap8 + j], p);
+    return true;
+  };
   if (n_tot > N) {
     const int ncand = n_tot - pcount;
     const int need = N - pcount;            // >= 0: N >= P >= pcount
     if (need <= 0) {
       mode = 1;
     } else if (ncand - need == 1) {
-      unsigned long long v = ~0ull;
-      for (int i = tid; i < n8 + n16; i += kThreads) {
-        const bool is8 = i < n8;
-        const int j = is8 ? i : i - n8;
-        const int p = is8 ? pos8[j] : pos16[j];
-        if (!is8 && t - p < P) continue;
-        const unsigned long long k = key64(keys[is8 ? j : cap8 + j], p);
-        v = k < v ? k : v;
+      if (!in_regs) {
+        lmin = ~0ull;
+        for (int i = tid; i < ntok; i += kThreads) {
+          unsigned long long k64;
+          if (cand_key(i, k64)) lmin = k64 < lmin ? k64 : lmin;
+        }
       }
-      kmin = block_min_u64(v, s_min);
+      kmin = block_min_u64(lmin, s_min);
       mode = 3;
     } else {
       mode = 2;
@@ -180,13 +258,17 @@ __global__ void __launch_bounds__(kThreads) k_select(Cache c, StepParams sp) {
         const int shift = 56 - 8 * pass;
         for (int i = tid; i < 256; i += kThreads) s_hist[i] = 0;
         __syncthreads();
-        for (int i = tid; i < n8 + n16; i += kThreads) {
-          const bool is8 = i < n8;
-          const int j = is8 ? i : i - n8;
-          const int p = is8 ? pos8[j] : pos16[j];
-          if (!is8 && t - p < P) continue;
-          const unsigned long long kk = key64(keys[is8 ? j : cap8 + j], p);
-          if ((kk & mask) == prefix) atomicAdd(&s_hist[(kk >> shift) & 255u], 1);
+        if (in_regs) {
+#pragma unroll
+          for (int r = 0; r < kReg; ++r)
+            if (rcand[r] && (rkey[r] & mask) == prefix)
+              atomicAdd(&s_hist[(rkey[r] >> shift) & 255u], 1);
+        } else {
+          for (int i = tid; i < ntok; i += kThreads) {
+            unsigned long long kk;
+            if (cand_key(i, kk) && (kk & mask) == prefix)
+              atomicAdd(&s_hist[(kk >> shift) & 255u], 1);
+          }
         }
         __syncthreads();
         if (tid == 0) {
@@ -209,107 +291,143 @@ __global__ void __launch_bounds__(kThreads) k_select(Cache c, StepParams sp) {
       }
     }
   }
-  auto kept = [&](bool is8, int j) -> bool {
-    const int p = is8 ? pos8[j] : pos16[j];
-    if (!is8 && t - p < P) return true;
+  auto keep_key = [&](unsigned long long kk) -> bool {
     if (mode == 0) return true;
     if (mode == 1) return false;
-    const unsigned long long kk = key64(keys[is8 ? j : cap8 + j], p);
     if (mode == 2) return (kk & mask) >= prefix;
     return kk != kmin;
   };
 
-  // ---- phase B: compaction plan of the INT8 region ----
-  const bool keptA = (jage >= 0) && kept(false, jage);
-  int k8 = 0;
-  {
-    int dummy = 0, tot = 0, tot2 = 0;
-    for (int base = 0; base < n8; base += kThreads) {
-      const int j = base + tid;
-      int r1, r2;
-      block_scan2(j < n8 && kept(true, j), false, s_wsum, r1, r2, tot, tot2);
-      (void)r1; (void)r2; (void)dummy;
-    }
-    k8 = tot;
-  }
-  const int n8n = k8 + (keptA ? 1 : 0);
-  int nmov8 = 0;
-  {
-    int toth = 0, totm = 0;
-    const int lim = max(n8, n8n);
-    int2* jobs = c.jobs8 + static_cast<size_t>(lb) * cap8;
-    for (int base = 0; base < lim; base += kThreads) {
-      const int j = base + tid;
-      const bool hole = (j < n8n) && (j >= n8 || !kept(true, j));
-      const bool mover = (j >= n8n) && (j < n8) && kept(true, j);
-      int rh, rm;
-      block_scan2(hole, mover, s_wsum, rh, rm, toth, totm);
-      if (hole) jobs[rh].x = j;
-      if (mover) jobs[rm].y = j;
-    }
-    nmov8 = totm;
-  }
-  // ---- FP16 region ----
-  int k16 = 0;
-  {
-    int tot = 0, tot2 = 0;
-    for (int base = 0; base < n16; base += kThreads) {
-      const int j = base + tid;
-      int r1, r2;
-      block_scan2(j < n16 && j != jage && kept(false, j), false, s_wsum, r1, r2, tot, tot2);
-    }
-    k16 = tot;
-  }
-  const int n16n = k16 + 1;
-  int nmov16 = 0;
-  {
-    int toth = 0, totm = 0;
-    const int lim = max(n16, n16n);
-    int2* jobs = c.jobs16 + static_cast<size_t>(lb) * c.Wr;
-    for (int base = 0; base < lim; base += kThreads) {
-      const int j = base + tid;
-      const bool kn = (j < n16) && j != jage && kept(false, j);
-      const bool hole = (j < n16n) && !kn;
-      const bool mover = (j >= n16n) && kn;
-      int rh, rm;
-      block_scan2(hole, mover, s_wsum, rh, rm, toth, totm);
-      if (hole) jobs[rh].x = j;
-      if (mover) jobs[rm].y = j;
-    }
-    nmov16 = totm;
-    if (tid == 0) jobs[nmov16].y = -1;      // the new token fills the last hole
+  // ---- keep flags in shared memory: one pass over the slots ----
+  // fl8[j]: INT8 slot j kept; fl16[j]: FP16 slot j kept and staying FP16
+  extern __shared__ __align__(16) unsigned char fl[];
+  unsigned char* fl8 = fl;
+  unsigned char* fl16 = fl + cap8;
+  int2* sj8 = reinterpret_cast<int2*>(fl + ((cap8 + c.Wr + 15) & ~15));   // [Ncap + 1]
+  int2* sj16 = sj8 + c.Ncap + 1;                                            // [Wr]
+  __shared__ int s_k8, s_k16, s_keptA;
+  if (tid == 0) {
+    s_k8 = 0;
+    s_k16 = 0;
+    s_keptA = 0;
   }
   __syncthreads();
+  {
+    int c8 = 0, c16 = 0;
+    auto flag = [&](int i, bool cand, unsigned long long kk) {
+      const bool k = !cand || keep_key(kk);
+      if (i < n8) {
+        fl8[i] = k;
+        c8 += k;
+      } else {
+        const int j = i - n8;
+        if (j == jage) {
+          s_keptA = k;
+          fl16[j] = 0;
+        } else {
+          fl16[j] = k;
+          c16 += k;
+        }
+      }
+    };
+    if (in_regs) {
+#pragma unroll
+      for (int r = 0; r < kReg; ++r) {
+        const int i = r * kThreads + tid;
+        if (i < ntok) flag(i, rcand[r], rkey[r]);
+      }
+    } else {
+      for (int i = tid; i < ntok; i += kThreads) {
+        unsigned long long kk = 0;
+        const bool cand = cand_key(i, kk);
+        flag(i, cand, kk);
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      c8 += __shfl_xor_sync(0xffffffffu, c8, o);
+      c16 += __shfl_xor_sync(0xffffffffu, c16, o);
+    }
+    if ((tid & 31) == 0) {
+      atomicAdd(&s_k8, c8);
+      atomicAdd(&s_k16, c16);
+    }
+  }
+  __syncthreads();
+  const bool keptA = s_keptA != 0;
+  const int n8n = s_k8 + (keptA ? 1 : 0);
+  const int n16n = s_k16 + 1;
+  // ---- compaction plans: hole of rank r <- mover of rank r ----
+  const int nmov8 = plan_region(fl8, n8, n8n, sj8, s_wsum);
+  const int nmov16 = plan_region(fl16, n16, n16n, sj16, s_wsum);
+  if (tid == 0) sj16[nmov16].y = -1;        // the new token fills the last FP16 hole
+  __syncthreads();
 
-  // ---- phase C: metadata moves (INT8 destinations first: the aging token is
-  // read from its FP16 slot before any FP16 slot is overwritten) ----
-  const int2* j8 = c.jobs8 + static_cast<size_t>(lb) * cap8;
-  const int2* j16 = c.jobs16 + static_cast<size_t>(lb) * c.Wr;
+  // ---- phase C: data and metadata moves.  INT8 destinations first: the
+  // aging token is read from its FP16 slot before FP16 slots are rewritten ----
+  const int2* j8 = sj8;
+  const int2* j16 = sj16;
+  const int d = c.d;
+  const int warp = tid >> 5, lane = tid & 31;
+  {
+    // one warp per (move, KV head): lanes copy the 16-byte pieces of the K and
+    // V rows, two more lanes the two scales
+    const int cpr = d / 16;
+    for (int p = warp; p < nmov8 * Hkv; p += kWarps) {
+      const int r = p / Hkv, h = p - r * Hkv;
+      const int2 jb = j8[r];
+      const size_t u8 = (static_cast<size_t>(lb) * Hkv + h) * cap8;
+      if (lane < 2 * cpr) {
+        int8_t* base = (lane < cpr ? c.k8 : c.v8) + u8 * d;
+        const int ch = lane < cpr ? lane : lane - cpr;
+        reinterpret_cast<int4*>(base + static_cast<size_t>(jb.x) * d)[ch] =
+            reinterpret_cast<const int4*>(base + static_cast<size_t>(jb.y) * d)[ch];
+      } else if (lane < 2 * cpr + 2) {
+        float* sc = (lane == 2 * cpr) ? c.ks : c.vs;
+        sc[u8 + jb.x] = sc[u8 + jb.y];
+      }
+    }
+  }
   for (int r = tid; r < nmov8; r += kThreads) {
     const int2 jb = j8[r];
     pos8[jb.x] = pos8[jb.y];
     ema8[jb.x] = ema8[jb.y];
   }
-  int hage = -1;
-  if (keptA) hage = j8[nmov8].x;
-  if (keptA && tid == 0) {
-    pos8[hage] = pos16[jage];
-    ema8[hage] = ema16[jage];
-  }
-  // the aging token's K/V rows: quantise FP16 slot jage into INT8 slot hage
   if (keptA) {
-    const int warp = tid >> 5;
+    const int hage = j8[nmov8].x;
+    if (tid == 0) {
+      pos8[hage] = pos16[jage];
+      ema8[hage] = ema16[jage];
+    }
+    // the aging token's K/V rows: quantise FP16 slot jage into INT8 slot hage
     for (int row = warp; row < 2 * Hkv; row += kWarps) {
       const int h = row >> 1;
       const bool isv = row & 1;
       const size_t u8 = static_cast<size_t>(lb) * Hkv + h;
-      const __half* src = (isv ? c.v16 : c.k16) + (u8 * c.Wr + jage) * c.d;
-      int8_t* dst = (isv ? c.v8 : c.k8) + (u8 * cap8 + hage) * c.d;
+      const __half* src = (isv ? c.v16 : c.k16) + (u8 * c.Wr + jage) * d;
+      int8_t* dst = (isv ? c.v8 : c.k8) + (u8 * cap8 + hage) * d;
       float* sc = (isv ? c.vs : c.ks) + u8 * cap8 + hage;
-      quantize_row_warp(src, dst, sc, c.d);
+      quantize_row_warp(src, dst, sc, d);
     }
   }
   __syncthreads();
+  {
+    // one warp per (FP16 move or new token, KV head): one lane per 16-byte piece
+    const int cpr = d / 8;
+    for (int p = warp; p < (nmov16 + 1) * Hkv; p += kWarps) {
+      const int r = p / Hkv, h = p - r * Hkv;
+      if (lane < 2 * cpr) {
+        const int2 jb = j16[r];
+        const size_t u8 = static_cast<size_t>(lb) * Hkv + h;
+        const bool isv = lane >= cpr;
+        const int ch = isv ? lane - cpr : lane;
+        __half* base = (isv ? c.v16 : c.k16) + u8 * c.Wr * d;
+        const __half* src = (jb.y >= 0) ? base + static_cast<size_t>(jb.y) * d
+                                        : (isv ? sp.v_new : sp.k_new) + u8 * d;
+        reinterpret_cast<int4*>(base + static_cast<size_t>(jb.x) * d)[ch] =
+            reinterpret_cast<const int4*>(src)[ch];
+      }
+    }
+  }
   for (int r = tid; r < nmov16; r += kThreads) {
     const int2 jb = j16[r];
     pos16[jb.x] = pos16[jb.y];
@@ -324,16 +442,25 @@ __global__ void __launch_bounds__(kThreads) k_select(Cache c, StepParams sp) {
 
   // ---- outputs ----
   if (sp.kept_pos) {
-    int32_t* kp = sp.kept_pos + static_cast<size_t>(lb) * c.Ncap;
-    for (int j = tid; j < n8n; j += kThreads) kp[j] = pos8[j];
-    for (int j = tid; j < n16n; j += kThreads) kp[n8n + j] = pos16[j];
+    int32_t* __restrict__ kp = sp.kept_pos + static_cast<size_t>(lb) * c.Ncap;
+    for (int base = 0; base < n8n + n16n; base += 4 * kThreads) {
+      int v[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = base + r * kThreads + tid;
+        v[r] = (i < n8n) ? pos8[i] : (i < n8n + n16n ? pos16[i - n8n] : 0);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = base + r * kThreads + tid;
+        if (i < n8n + n16n) kp[i] = v[r];
+      }
+    }
   }
   if (tid == 0) {
     if (sp.kept_count) sp.kept_count[lb] = n8n + n16n;
     c.n8[lb] = n8n;
     c.n16[lb] = n16n;
-    c.njobs[lb * 2] = nmov8;
-    c.njobs[lb * 2 + 1] = nmov16 + 1;
     atomicAdd(&c.stats->evicted, static_cast<unsigned long long>(n_tot - n8n - n16n));
     atomicAdd(&c.stats->quantized, keptA ? 1ull : 0ull);
     atomicAdd(&c.stats->moved, static_cast<unsigned long long>(nmov8 + nmov16));
@@ -347,7 +474,16 @@ __global__ void __launch_bounds__(kThreads) k_select(Cache c, StepParams sp) {
 }  // namespace
 
 cudaError_t launch_select(const Cache& c, const StepParams& sp, cudaStream_t s) {
-  k_select<<<c.L * c.B, kThreads, 0, s>>>(c, sp);
+  const size_t smem = ((static_cast<size_t>(c.cap8) + c.Wr + 15) & ~static_cast<size_t>(15)) +
+                      (static_cast<size_t>(c.Ncap) + 1 + c.Wr) * sizeof(int2);
+  static size_t attr = 48 * 1024;
+  if (smem > attr) {
+    const cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr = smem;
+  }
+  k_select<<<c.L * c.B, kThreads, smem, s>>>(c, sp);
   return cudaGetLastError();
 }
 
