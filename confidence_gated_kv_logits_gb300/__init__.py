@@ -44,7 +44,7 @@ class Opts(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("vocab", ctypes.c_int),
                 ("max_context", ctypes.c_int), ("pyramid_min", ctypes.c_float),
                 ("device", ctypes.c_int), ("attn_splits", ctypes.c_int),
-                ("attn_kernel", ctypes.c_int)]
+                ("attn_kernel", ctypes.c_int), ("attn_tma", ctypes.c_int)]
 
 
 class Stats(ctypes.Structure):
@@ -128,12 +128,13 @@ class ConfKV:
 
     def __init__(self, layers, heads, kv_heads, head_dim, N_low, N_high, tau, P, W,
                  ema_decay, *, batch=1, vocab, max_context=0, pyramid_min=1.0,
-                 device=None, attn_splits=0, attn_kernel=0):
+                 device=None, attn_splits=0, attn_kernel=0, attn_tma=0):
         import torch
         self._L = load_library()
         dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         self.device = dev
-        opts = Opts(batch, vocab, max_context, pyramid_min, dev.index, attn_splits, attn_kernel)
+        opts = Opts(batch, vocab, max_context, pyramid_min, dev.index, attn_splits, attn_kernel,
+                    attn_tma)
         h = ctypes.c_void_p()
         rc = self._L.confkv_create(layers, heads, kv_heads, head_dim, N_low, N_high, tau, P,
                                    W, ema_decay, ctypes.byref(opts), ctypes.byref(h))

@@ -70,6 +70,8 @@ struct confkv_ctx {
   float* st_conf = nullptr;
   int32_t* st_bud = nullptr;
   std::string msg = "ok";
+  alignas(64) unsigned char tmaps[512];          // tensor maps of the d = 128 TMA path
+  bool has_tmaps = false;
   // profiling
   int prof = 0;                                 // kernel bit mask
   std::vector<cudaEvent_t> ev[kProfKernels];   // start/stop pairs
@@ -140,6 +142,7 @@ int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s) {
   ap.q = q;
   ap.out = out;
   ap.kernel = c->attn_kernel;
+  ap.tmaps = c->has_tmaps ? c->tmaps : nullptr;
   ap.splits = c->splits;
   ap.part_ml = c->part_ml;
   ap.part_acc = c->part_acc;
@@ -168,7 +171,7 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
       W < P || N_low < P || N_high < P || !(ema_decay >= 0.0f && ema_decay <= 1.0f) ||
       !std::isfinite(tau) || o.batch < 1 || o.vocab < 2 || o.max_context < 0 ||
       !(pmin > 0.0f && pmin <= 1.0f) || o.attn_splits < 0 || o.attn_splits > 64 ||
-      o.attn_kernel < 0 || o.attn_kernel > 2 ||
+      o.attn_kernel < 0 || o.attn_kernel > 2 || o.attn_tma < -1 || o.attn_tma > 0 ||
       (o.attn_kernel == 2 && heads / kv_heads > 8))
     return CONFKV_ERR_INVALID_ARG;
   int dev = o.device;
@@ -250,6 +253,7 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
     e = cudaMemcpy(c->btab, bt.data(), bt.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess && c->d == 128 && o.attn_tma >= 0) c->has_tmaps = confkv::encode_attention_maps(c->cache, c->tmaps);
   if (e != cudaSuccess) {
     const bool oom = (e == cudaErrorMemoryAllocation);
     cudaGetLastError();

@@ -70,6 +70,7 @@ struct StepParams {
 
 struct AttnParams {
   int kernel;             // 0 auto, 1 CUDA-core, 2 tensor-core
+  const void* tmaps;     // host pointer to 4 CUtensorMap (K8, V8, K16, V16) or null
   const __half* q;       // [L*B][Hq][d]
   float* out;            // [L*B][Hq][d]
   int splits;
@@ -90,5 +91,8 @@ cudaError_t launch_prefill_store(const Cache& c, const __half* k, const __half* 
                                  cudaStream_t s);
 cudaError_t launch_attention(const Cache& c, const AttnParams& ap, cudaStream_t s);
 cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStream_t s);
+// Encodes the four tensor maps of the d = 128 TMA attention path into `out`
+// (4 CUtensorMap, 512 bytes); returns false if the driver cannot.
+bool encode_attention_maps(const Cache& c, void* out);
 
 }  // namespace confkv

@@ -26,7 +26,10 @@
 // tokens, 8 KB at d = 128) through a cp.async ring of kStages stages in a
 // thread-private shared-memory layout (conflict-free, no cross-lane data
 // except the 64 scales of an INT8 chunk).
+#include <cuda.h>
+
 #include <cfloat>
+#include <cstring>
 
 #include "confkv_internal.cuh"
 
@@ -133,6 +136,78 @@ __device__ __forceinline__ float pow2i(int e) {
   return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
+// ---- TMA (tensor-map tile loads, 128-byte swizzle) + mbarrier helpers ----
+constexpr int kTmaStage = 9216;                  // K tile 4 KB | V tile 4 KB | scales | pad
+constexpr unsigned kWaitSpins = 1u << 26;        // bounded mbarrier wait (then flag + bail)
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait: false when the copy never completed (the caller flags it)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, unsigned parity) {
+  for (unsigned i = 0; i < kWaitSpins; ++i)
+    if (mbar_try(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_1d(uint32_t dst, const void* src, unsigned bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// address of 16-byte chunk `ch` of row `row` in a 128-byte-swizzled tile
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int ch) {
+  return tile + static_cast<uint32_t>(row * 128 + ((ch ^ (row & 7)) << 4));
+}
+
+struct TmaMaps {
+  CUtensorMap k8, v8, k16, v16;
+};
+
+// TMA issue of one chunk (d = 128) by one lane: INT8 chunk = K and V tiles of
+// 32 rows x 128 B + the 2 x 32 scales; FP16 chunk = K and V tiles of 16 rows
+// x 256 B as two 128-byte-wide boxes each.
+__device__ __forceinline__ void issue_chunk_tma(const Cache& c, const TmaMaps& tm, int unit,
+                                                int nc8, int ci, uint32_t st, uint32_t bar) {
+  if (ci < nc8) {
+    const int row0 = unit * c.cap8 + 32 * ci;
+    mbar_expect_tx(bar, 2 * 4096 + 256);
+    tma_2d(st, &tm.k8, 0, row0, bar);
+    tma_2d(st + 4096, &tm.v8, 0, row0, bar);
+    bulk_1d(st + 8192, c.ks + row0, 128, bar);
+    bulk_1d(st + 8192 + 128, c.vs + row0, 128, bar);
+  } else {
+    const int row0 = unit * c.Wr + 16 * (ci - nc8);
+    mbar_expect_tx(bar, 2 * 4096);
+    tma_2d(st, &tm.k16, 0, row0, bar);
+    tma_2d(st + 2048, &tm.k16, 64, row0, bar);
+    tma_2d(st + 4096, &tm.v16, 0, row0, bar);
+    tma_2d(st + 6144, &tm.v16, 64, row0, bar);
+  }
+}
+
 // cp.async of one chunk into a stage.  INT8 chunk ci: slots 32ci..32ci+31
 // (two 16-token blocks); FP16 chunk: slots 16cf..16cf+15.
 template <int D>
@@ -191,10 +266,16 @@ struct SoftState {
   int E;                  // O holds values scaled by 2^E
 };
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 3) k_attn_mma(Cache c, AttnParams ap) {
+template <int D, bool TMA>
+__global__ void __launch_bounds__(kThreads, 3)
+k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   using G = Geo<D>;
-  extern __shared__ __align__(16) unsigned char smem[];
+  static_assert(!TMA || D == 128, "the TMA path is specialised for head_dim 128");
+  constexpr int STAGE = TMA ? kTmaStage : G::STAGE;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  // 1024-byte aligned base (128-byte swizzle atoms)
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
   const int unit = blockIdx.x, split = blockIdx.y;
   const int lb = unit / c.Hkv, kvh = unit - lb * c.Hkv, g = c.g;
   const int n8 = c.n8[lb], n16 = c.n16[lb];
@@ -203,8 +284,15 @@ __global__ void __launch_bounds__(kThreads, 3) k_attn_mma(Cache c, AttnParams ap
   const int ce = static_cast<int>(static_cast<long long>(nc) * (split + 1) / ap.splits);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, t4 = lane & 3;
   const int cnt = (ce - cb > warp) ? (ce - cb - warp + kWarps - 1) / kWarps : 0;
-  const uint32_t wbase = smem_u32(smem) + warp * kStages * G::STAGE;
-  const float* fbase = reinterpret_cast<const float*>(smem + warp * kStages * G::STAGE);
+  const uint32_t wbase = smem_u32(smem) + warp * kStages * STAGE;
+  if constexpr (TMA) {
+    if (lane == 0)
+      for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    __syncwarp();
+  }
+  bool ok_all = true;
+  int fail_i = 0;
 
   // Q^T operand: query gid, channels t4*KPT + 4kk + {0,1} and {2,3}
   uint32_t qb[G::KS][2];
@@ -294,25 +382,37 @@ __global__ void __launch_bounds__(kThreads, 3) k_attn_mma(Cache c, AttnParams ap
   };
 
   // ---- main loop over this warp's chunks ----
-#pragma unroll
-  for (int i = 0; i < kStages - 1; ++i) {
-    if (i < cnt) issue_chunk<D>(c, unit, nc8, cb + warp + kWarps * i, wbase + i * G::STAGE, lane);
-    cp_commit();
-  }
-  for (int i = 0; i < cnt; ++i) {
-    cp_wait<kStages - 2>();
-    __syncwarp();
-    {
-      const int nx = i + kStages - 1;
-      if (nx < cnt)
-        issue_chunk<D>(c, unit, nc8, cb + warp + kWarps * nx, wbase + (nx % kStages) * G::STAGE, lane);
+  auto issue = [&](int i) {
+    if constexpr (TMA) {
+      if (lane == 0 && i < cnt) {
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        issue_chunk_tma(c, tm, unit, nc8, cb + warp + kWarps * i, wbase + (i % kStages) * STAGE,
+                        smem_u32(&bars[warp][i % kStages]));
+      }
+    } else {
+      if (i < cnt) issue_chunk<D>(c, unit, nc8, cb + warp + kWarps * i, wbase + (i % kStages) * STAGE, lane);
       cp_commit();
     }
+  };
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) issue(i);
+  for (int i = 0; i < cnt; ++i) {
+    if constexpr (TMA) {
+      if (!mbar_wait(smem_u32(&bars[warp][i % kStages]), (i / kStages) & 1)) {
+        ok_all = false;
+        fail_i = i;
+        break;
+      }
+    } else {
+      cp_wait<kStages - 2>();
+    }
+    __syncwarp();
+    issue(i + kStages - 1);
     const int ci = cb + warp + kWarps * i;
-    const uint32_t st = wbase + (i % kStages) * G::STAGE;
+    const uint32_t st = wbase + (i % kStages) * STAGE;
     if (ci < nc8) {
       // ------------------------- INT8 chunk: 32 tokens -------------------------
-      const uint32_t sks = st + G::DATA, svs = sks + 128;
+      const uint32_t sks = st + (TMA ? 8192 : G::DATA), svs = sks + 128;
       const int tb = 32 * ci;
       uint32_t kw[2][2][G::KS];
 #pragma unroll
@@ -321,7 +421,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_attn_mma(Cache c, AttnParams ap
         for (int r = 0; r < 2; ++r)
 #pragma unroll
           for (int u = 0; u < G::KPT / 16; ++u) {
-            const uint4 v = lds128(tp(st, lane, (2 * sb + r) * G::KPT + 16 * u));
+            const uint4 v = TMA ? lds128(swz(st, 16 * sb + gid + 8 * r, 2 * t4 + u))
+                                : lds128(tp(st, lane, (2 * sb + r) * G::KPT + 16 * u));
             kw[sb][r][4 * u] = v.x;
             kw[sb][r][4 * u + 1] = v.y;
             kw[sb][r][4 * u + 2] = v.z;
@@ -384,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_attn_mma(Cache c, AttnParams ap
         for (int ii = 0; ii < 4; ++ii) {
           const int b = D + (4 * sb + ii) * G::VPT;
           if constexpr (G::VPT == 16) {
-            const uint4 v = lds128(tp(st, lane, b));
+            const int row = 16 * sb + 2 * t4 + (ii & 1) + 8 * (ii >> 1);
+            const uint4 v = TMA ? lds128(swz(st + 4096, row, gid)) : lds128(tp(st, lane, b));
             vw[ii][0] = v.x;
             vw[ii][1] = v.y;
             vw[ii][2] = v.z;
@@ -405,7 +507,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_attn_mma(Cache c, AttnParams ap
       for (int r = 0; r < 2; ++r)
 #pragma unroll
         for (int u = 0; u < G::KPT / 8; ++u) {
-          const uint4 v = lds128(tp(st, lane, r * G::KPT * 2 + 16 * u));
+          const uint4 v = TMA ? lds128(swz(st + 2048 * (t4 >> 1), gid + 8 * r, 4 * (t4 & 1) + u))
+                              : lds128(tp(st, lane, r * G::KPT * 2 + 16 * u));
           kw[r][4 * u] = v.x;
           kw[r][4 * u + 1] = v.y;
           kw[r][4 * u + 2] = v.z;
@@ -450,7 +553,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_attn_mma(Cache c, AttnParams ap
       for (int ii = 0; ii < 4; ++ii)
 #pragma unroll
         for (int u = 0; u < G::VPT / 8; ++u) {
-          const uint4 v = lds128(tp(st, lane, D + ii * G::VPT * 2 + 16 * u));
+          const int row = 2 * t4 + (ii & 1) + 8 * (ii >> 1);
+          const uint4 v = TMA ? lds128(swz(st + 4096 + 2048 * (gid >> 2), row, 2 * (gid & 3) + u))
+                              : lds128(tp(st, lane, D + ii * G::VPT * 2 + 16 * u));
           vw[ii][4 * u] = v.x;
           vw[ii][4 * u + 1] = v.y;
           vw[ii][4 * u + 2] = v.z;
@@ -466,7 +571,14 @@ __global__ void __launch_bounds__(kThreads, 3) k_attn_mma(Cache c, AttnParams ap
       pv_f16(x, vw);
     }
   }
-  cp_wait<0>();
+  if constexpr (!TMA) cp_wait<0>();
+  if (!ok_all) {
+    // a tile never arrived: flag the step (its output for this unit is
+    // incomplete) and give the copy in flight one more bounded wait before
+    // the shared memory is reused
+    if (lane == 0) atomicOr(c.err, 4);
+    mbar_wait(smem_u32(&bars[warp][fail_i % kStages]), (fail_i / kStages) & 1);
+  }
 
   // ---- merge the warps of this CTA (shared memory reused) ----
   ss.lA = gsum8(ss.lA);
@@ -573,26 +685,84 @@ __global__ void __launch_bounds__(kThreads, 3) k_attn_mma(Cache c, AttnParams ap
   }
 }
 
-template <int D>
-cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, cudaStream_t s) {
-  const int smem = kWarps * kStages * Geo<D>::STAGE;
+template <int D, bool TMA>
+cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm, cudaStream_t s) {
+  const int smem = kWarps * kStages * (TMA ? kTmaStage : Geo<D>::STAGE) + (TMA ? 1024 : 0);
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(k_attn_mma<D>,
+    const cudaError_t e = cudaFuncSetAttribute(k_attn_mma<D, TMA>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k_attn_mma<D><<<dim3(c.L * c.B * c.Hkv, ap.splits), kThreads, smem, s>>>(c, ap);
+  k_attn_mma<D, TMA><<<dim3(c.L * c.B * c.Hkv, ap.splits), kThreads, smem, s>>>(c, ap, tm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+bool encode_attention_maps(const Cache& c, void* out) {
+  if (c.d != 128) return false;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+  Encode enc = reinterpret_cast<Encode>(fn);
+  TmaMaps tm;
+  std::memset(&tm, 0, sizeof(tm));
+  const cuuint64_t units = static_cast<cuuint64_t>(c.L) * c.B * c.Hkv;
+  const cuuint32_t estr[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {128, units * c.cap8};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, 32};
+    if (enc(&tm.k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.k8, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+    if (enc(&tm.v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.v8, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  {
+    const cuuint64_t dims[2] = {128, units * c.Wr};
+    const cuuint64_t strides[1] = {256};
+    const cuuint32_t box[2] = {64, 16};
+    if (enc(&tm.k16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c.k16, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+    if (enc(&tm.v16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c.v16, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  std::memcpy(out, &tm, sizeof(tm));
+  return true;
+}
+
 cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStream_t s) {
   if (c.g < 1 || c.g > 8) return cudaErrorInvalidValue;
-  if (c.d == 64) return launch_mma_d<64>(c, ap, s);
-  if (c.d == 128) return launch_mma_d<128>(c, ap, s);
+  TmaMaps tm;
+  if (c.d == 64) {
+    std::memset(&tm, 0, sizeof(tm));
+    return launch_mma_d<64, false>(c, ap, tm, s);
+  }
+  if (c.d == 128) {
+    if (ap.tmaps) {
+      std::memcpy(&tm, ap.tmaps, sizeof(tm));
+      return launch_mma_d<128, true>(c, ap, tm, s);
+    }
+    std::memset(&tm, 0, sizeof(tm));
+    return launch_mma_d<128, false>(c, ap, tm, s);
+  }
   return cudaErrorInvalidValue;
 }
 

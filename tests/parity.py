@@ -76,7 +76,7 @@ def compare_cache(kv, orc, l, b, rep):
 
 
 def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, splits=0,
-        logits_override=None, kernel=0):
+        logits_override=None, kernel=0, tma=0):
     """Run workload `w` on the GPU and in the oracle; return a Report.
 
     lbs: iterable of (l, b) the oracle simulates (default: all).
@@ -87,7 +87,8 @@ def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, spli
     import confidence_gated_kv_logits_gb300 as pkg
     dev = torch.device("cuda", 0)
     steps = w.steps if steps is None else steps
-    kv = pkg.ConfKV.for_workload(w, device=0, attn_splits=splits, attn_kernel=kernel)
+    kv = pkg.ConfKV.for_workload(w, device=0, attn_splits=splits, attn_kernel=kernel,
+                                attn_tma=tma)
     orc = oracle.Oracle.for_workload(w)
     all_lbs = [(l, b) for l in range(w.L) for b in range(w.B)]
     lbs = all_lbs if lbs is None else list(lbs)

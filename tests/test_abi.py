@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_invalid_arguments_rejected_on_host(lib):
     import confidence_gated_kv_logits_gb300 as pkg
     h = ctypes.c_void_p()
-    o = pkg.Opts(1, 1000, 0, 1.0, -1, 0, 0)
+    o = pkg.Opts(1, 1000, 0, 1.0, -1, 0, 0, 0)
     good = (2, 8, 2, 128, 36, 24, 0.5, 4, 16, 0.9)
     bad_cases = [
         (2, 8, 3, 128, 36, 24, 0.5, 4, 16, 0.9),    # Hq % Hkv != 0
@@ -55,11 +55,11 @@ def test_invalid_arguments_rejected_on_host(lib):
     for args in bad_cases:
         rc = lib.confkv_create(*args, ctypes.byref(o), ctypes.byref(h))
         assert rc == pkg.ERR_INVALID_ARG and not h.value, args
-    o_bad = pkg.Opts(1, 1, 0, 1.0, -1, 0, 0)                 # vocab < 2
+    o_bad = pkg.Opts(1, 1, 0, 1.0, -1, 0, 0, 0)                 # vocab < 2
     assert lib.confkv_create(*good, ctypes.byref(o_bad), ctypes.byref(h)) == pkg.ERR_INVALID_ARG
-    o_bad = pkg.Opts(1, 1000, 0, 1.5, -1, 0, 0)              # pyramid factor > 1
+    o_bad = pkg.Opts(1, 1000, 0, 1.5, -1, 0, 0, 0)              # pyramid factor > 1
     assert lib.confkv_create(*good, ctypes.byref(o_bad), ctypes.byref(h)) == pkg.ERR_INVALID_ARG
-    o_bad = pkg.Opts(1, 1000, 0, 1.0, -1, 0, 3)             # unknown kernel choice
+    o_bad = pkg.Opts(1, 1000, 0, 1.0, -1, 0, 3, 0)             # unknown kernel choice
     assert lib.confkv_create(*good, ctypes.byref(o_bad), ctypes.byref(h)) == pkg.ERR_INVALID_ARG
     assert lib.confkv_create(*good, ctypes.byref(o), None) == pkg.ERR_INVALID_ARG
     # null contexts

@@ -133,19 +133,19 @@ def test_gqa8_d64_pyramid():
 
 
 @pytest.mark.parametrize("splits", [1, 3])
-@pytest.mark.parametrize("kernel", [1, 2])
-def test_forced_split_counts_and_kernels(splits, kernel):
+@pytest.mark.parametrize("kernel,tma", [(1, 0), (2, 0), (2, -1)])
+def test_forced_split_counts_and_kernels(splits, kernel, tma):
     w = small(prefill=90, steps=40, V=64)
-    _check(parity.run(w, splits=splits, kernel=kernel))
+    _check(parity.run(w, splits=splits, kernel=kernel, tma=tma))
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel,tma", [(1, 0), (2, 0), (2, -1)])
 @pytest.mark.parametrize("Hq,Hkv,d", [(12, 12, 64), (40, 8, 128), (64, 8, 64), (6, 2, 128),
-                                      (7, 1, 64)])
-def test_attention_kernels_over_group_sizes(kernel, Hq, Hkv, d):
+                                      (7, 1, 64), (16, 2, 128)])
+def test_attention_kernels_over_group_sizes(kernel, tma, Hq, Hkv, d):
     w = small(L=1, B=2, Hq=Hq, Hkv=Hkv, d=d, prefill=77, steps=25, N_high=40, N_low=60,
               P=5, W=19, V=64)
-    _check(parity.run(w, kernel=kernel))
+    _check(parity.run(w, kernel=kernel, tma=tma))
 
 
 def test_large_values_and_scale_extremes():
