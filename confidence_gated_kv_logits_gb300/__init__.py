@@ -31,7 +31,8 @@ FLAG_TIMEOUT = 4
 # every symbol declared in include/confkv.h
 EXPORTS = ("confkv_create", "confkv_prefill", "confkv_step", "confkv_step_host",
            "confkv_stats", "confkv_read_cache", "confkv_profile_enable",
-           "confkv_profile_read", "confkv_last_error", "confkv_free")
+           "confkv_profile_read", "confkv_last_error", "confkv_free",
+           "confkv_confidence_noalloc")
 
 
 class ConfKVError(RuntimeError):
@@ -98,6 +99,8 @@ def load_library(path=LIB_PATH):
     L.confkv_last_error.argtypes = [vp]
     L.confkv_free.restype = None
     L.confkv_free.argtypes = [vp]
+    L.confkv_confidence_noalloc.restype = ci
+    L.confkv_confidence_noalloc.argtypes = [vp, ci, ci, cf, ci, ci, vp, vp, vp, vp]
     _lib = L
     return L
 

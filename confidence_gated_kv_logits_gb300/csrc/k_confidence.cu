@@ -17,6 +17,10 @@
 // well inside the 1e-5 tolerance on c.  With p_i = e^(z_i - z*)/S:
 //   H = ln S - T/S,  p(1) = 1/S,  m = z(1) - z(2).
 #include <cfloat>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/confkv.h"
 
 #include "confkv_internal.cuh"
 
@@ -180,4 +184,152 @@ cudaError_t launch_confidence(const float* logits, int B, int V, float tau, int 
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the confidence and budget of a batch of logits
+// without a context and without any device allocation.  Its cross-CTA scratch
+// (one partial state per CTA and one ticket per sequence) lives in a
+// file-scope device array that every GPU loading this library holds until the
+// process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kNoAllocMaxBatch = 1024;           // sequences per call
+constexpr int kNoAllocMaxParts = 2048;           // CTAs per call (batch x CTAs per sequence)
+constexpr size_t kNoAllocBytes =
+    sizeof(ConfPart) * kNoAllocMaxParts + sizeof(unsigned int) * kNoAllocMaxBatch;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_conf_scratch[kNoAllocBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_conf_scratch on the current device: looked up once per
+// device with that device current (host code cannot use the symbol itself).
+cudaError_t scratch_address(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_conf_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+__global__ void __launch_bounds__(kThreads)
+k_confidence_noalloc(const float* __restrict__ logits, int V, int cps, float tau, int N_low,
+                     int N_high, float* conf_out, int32_t* budget_out, int32_t* flags_out,
+                     ConfPart* part, unsigned int* ticket) {
+  const int b = blockIdx.x / cps;
+  const int rk = blockIdx.x - b * cps;
+  const long long lo = static_cast<long long>(V) * rk / cps;
+  const long long hi_ = static_cast<long long>(V) * (rk + 1) / cps;
+  const float* z = logits + static_cast<size_t>(b) * V + lo;
+  const int Vc = static_cast<int>(hi_ - lo);
+  ConfState s{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
+  for (int base = 0; base < Vc; base += kBatch * kThreads) {
+    float x[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int i = base + k * kThreads + threadIdx.x;
+      x[k] = (i < Vc) ? __ldcs(z + i) : -INFINITY;
+    }
+    ConfState bs{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
+    int bad = 0;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      bad |= !(x[k] < INFINITY) && !(x[k] == -INFINITY);
+      bs.m2 = fmaxf(bs.m2, fminf(bs.m1, x[k]));
+      bs.m1 = fmaxf(bs.m1, x[k]);
+    }
+    bs.bad = bad;
+    if (bs.m1 > -INFINITY) {
+      const float ml = bs.m1 * kL2E;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const float xc = fmaxf(x[k], -3.0e38f);
+        const float e = ex2(fmaf(xc, kL2E, -ml));
+        bs.S += e;
+        bs.T = fmaf(e, xc - bs.m1, bs.T);
+      }
+    }
+    s = merge(s, bs);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s = merge(s, shfl_xor(s, o));
+  __shared__ ConfState sh[kThreads / 32];
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) sh[warp] = s;
+  __syncthreads();
+  if (warp == 0) {
+    s = (lane < kThreads / 32) ? sh[lane] : ConfState{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s = merge(s, shfl_xor(s, o));
+    if (lane == 0) {
+      part[blockIdx.x] = ConfPart{s.m1, s.m2, s.S, s.T, s.bad};
+      __threadfence();
+      s_last = (atomicAdd(&ticket[b], 1u) == static_cast<unsigned>(cps - 1));
+    }
+  }
+  __syncthreads();
+  if (!s_last || warp != 0) return;
+  __threadfence();
+  s = ConfState{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
+  for (int i = lane; i < cps; i += 32) {
+    const ConfPart* pp = part + static_cast<size_t>(b) * cps + i;
+    ConfState q{__ldcg(&pp->m1), __ldcg(&pp->m2), __ldcg(&pp->S), __ldcg(&pp->T), __ldcg(&pp->bad)};
+    s = merge(s, q);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s = merge(s, shfl_xor(s, o));
+  if (lane == 0) {
+    ticket[b] = 0u;
+    float c = 0.0f;
+    const bool bad = s.bad || !(s.S > 0.0f);
+    if (!bad) {
+      const float H = logf(s.S) - s.T / s.S;
+      const float Hn = H / logf(static_cast<float>(V));
+      const float m = s.m1 - s.m2;
+      const float sig = 1.0f / (1.0f + expf(-m));
+      c = 0.4f * (1.0f - Hn) + 0.3f * sig + 0.3f / s.S;
+    }
+    conf_out[b] = c;
+    if (budget_out) budget_out[b] = (!bad && c >= tau) ? N_high : N_low;
+    if (flags_out) flags_out[b] = bad ? CONFKV_FLAG_NONFINITE : 0;
+  }
+}
+
+}  // namespace
+
 }  // namespace confkv
+
+extern "C" int confkv_confidence_noalloc(const float* logits, int batch, int vocab, float tau,
+                                         int N_low, int N_high, float* conf_out,
+                                         int32_t* budget_out, int32_t* flags_out, void* stream) {
+  using namespace confkv;
+  if (!logits || !conf_out || batch < 1 || vocab < 2 || !std::isfinite(tau))
+    return CONFKV_ERR_INVALID_ARG;
+  const int cps = confidence_ctas_per_seq(batch, vocab);
+  if (batch > kNoAllocMaxBatch || static_cast<long long>(batch) * cps > kNoAllocMaxParts)
+    return CONFKV_ERR_CAPACITY;
+  void* base = nullptr;
+  if (scratch_address(&base) != cudaSuccess) return CONFKV_ERR_CUDA;
+  ConfPart* part = static_cast<ConfPart*>(base);
+  unsigned int* ticket = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(base) +
+                                                         sizeof(ConfPart) * kNoAllocMaxParts);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the tickets must start at zero; the partial states are written before read
+  if (cudaMemsetAsync(ticket, 0, sizeof(unsigned int) * batch, s) != cudaSuccess)
+    return CONFKV_ERR_CUDA;
+  k_confidence_noalloc<<<batch * cps, kThreads, 0, s>>>(logits, vocab, cps, tau, N_low, N_high,
+                                                        conf_out, budget_out, flags_out, part,
+                                                        ticket);
+  return cudaGetLastError() == cudaSuccess ? CONFKV_OK : CONFKV_ERR_CUDA;
+}

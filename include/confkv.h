@@ -205,6 +205,35 @@ int confkv_read_cache(confkv_ctx* ctx, int l, int b, int cap, int* n8, int* n16,
 int confkv_profile_enable(confkv_ctx* ctx, int kernel_mask);
 int confkv_profile_read(confkv_ctx* ctx, confkv_profile_t* out);
 
+/*
+ * confkv_confidence_noalloc -- the confidence c and budget of each of `batch`
+ * sequences, like the first stage of confkv_step, for callers that cannot
+ * allocate device memory: code that runs inside a fixed device-memory budget
+ * owned by someone else, a host process whose allocator must not be re-entered
+ * from this call, or a latency-critical loop that cannot absorb an
+ * allocation's cost or failure.  It needs no context and allocates nothing.
+ * The CONF-KV pages have no counterpart to this call; it is an engineering
+ * variant of the confidence reduction.
+ *   logits:     fp32 [batch][vocab] (device)
+ *   conf_out:   fp32 [batch] (device, required)
+ *   budget_out: int32 [batch] (device, may be NULL): N_high if c >= tau else N_low
+ *   flags_out:  int32 [batch] (device, may be NULL): CONFKV_FLAG_NONFINITE for a
+ *               row with a NaN/+inf logit or no finite logit (its c is 0)
+ * Work is enqueued on `stream` on the current device.  The cross-CTA scratch
+ * is a fixed device array inside the library (about 45 KB, held by every GPU
+ * that loads the library until the process exits): batch <= 1024 and at most
+ * 2048 CTAs per call, else CONFKV_ERR_CAPACITY before anything is enqueued.
+ * Every call shares that array, so calls whose work overlaps on the GPU (on
+ * different streams, or from several host threads) race; serialise them.
+ * The first call on each device looks up the array's device address (a
+ * one-time set-up with that device current); make that first call before any
+ * stream capture.  Returns CONFKV_OK, CONFKV_ERR_INVALID_ARG,
+ * CONFKV_ERR_CAPACITY or CONFKV_ERR_CUDA.
+ */
+int confkv_confidence_noalloc(const float* logits, int batch, int vocab, float tau,
+                              int N_low, int N_high, float* conf_out, int32_t* budget_out,
+                              int32_t* flags_out, void* stream);
+
 /* Message of the last error of this context (never NULL). */
 const char* confkv_last_error(const confkv_ctx* ctx);
 
