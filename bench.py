@@ -50,6 +50,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--layers", type=int, default=0,
                    help="profiling only: override the layer count (smaller capture)")
+    p.add_argument("--step-bytes", action="store_true",
+                   help="profiling only: run warmup+steps decode steps and print each "
+                        "step's algorithmic attention bytes (synchronises every step)")
     return p.parse_args()
 
 
@@ -470,10 +473,44 @@ def run_ours(args):
     return 0
 
 
+def run_step_bytes(args):
+    """Per-step algorithmic attention bytes, to pair an ncu capture of one
+    attention launch with the bytes that launch had to read."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import confidence_gated_kv_logits_gb300 as pkg
+    from synth import device as sd, workloads as wl
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = get_workload(args)
+    kv = pkg.ConfKV.for_workload(w)
+    if w.prefill:
+        Kp, Vp = sd.prefill_kv(w)
+        ql = wl.q_last(w)
+        kv.prefill(Kp, Vp, w.prefill, None if ql is None else torch.from_numpy(ql).to(dev))
+        del Kp, Vp
+    out = torch.empty(w.L, w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+    bufs = None
+    prev = kv.stats()[0]["attn_kv_bytes"]
+    for s in range(args.warmup + args.steps):
+        bufs = sd.step_inputs(w, s, bufs)
+        kv.step(*bufs, out)
+        st, _ = kv.stats()
+        print(json.dumps({"workload": w.name, "step": s, "attention_launch": s,
+                          "attn_alg_bytes": st["attn_kv_bytes"] - prev}), flush=True)
+        prev = st["attn_kv_bytes"]
+    kv.close()
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.step_bytes:
+        return run_step_bytes(args)
     return run_ours(args)
 
 
