@@ -452,7 +452,9 @@ int confkv_read_cache(confkv_ctx* c, int l, int b, int cap, int* n8o, int* n16o,
       if (dst8 && r8) {
         cp(t8.data(), (which ? c->cache.v8 : c->cache.k8) + u * c->cap8 * d, static_cast<size_t>(r8) * d);
         for (int i = 0; i < r8; ++i)
-          std::memcpy(dst8 + (static_cast<size_t>(i) * H + h) * d, t8.data() + static_cast<size_t>(i) * d, d);
+          for (int x = 0; x < d; ++x)   // stored offset binary (code + 128)
+            dst8[(static_cast<size_t>(i) * H + h) * d + x] =
+                static_cast<int8_t>(t8[static_cast<size_t>(i) * d + x] ^ 0x80);
       }
       float* dsts = which ? vs : ks;
       if (dsts && r8) {

@@ -1,7 +1,8 @@
 // Internal device-side layout of the CONF-KV cache and launch wrappers.
 //
 // HBM layout of one context (lb = l*B + b, h = KV head):
-//   INT8 region   k8, v8  int8  [L*B][Hkv][cap8][d]    (slots 0..n8-1 live)
+//   INT8 region   k8, v8  int8  [L*B][Hkv][cap8][d]    (slots 0..n8-1 live; each
+//                 byte holds code + 128 (offset binary), code in [-127, 127])
 //                 ks, vs  fp32  [L*B][Hkv][cap8]       one absmax scale per row
 //   FP16 region   k16,v16 fp16  [L*B][Hkv][Wr][d]      (slots 0..n16-1 live;
 //                 Wr = W rounded up to 16, so whole 16-token chunks stay in bounds)

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
           const int ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float x = static_cast<float>(static_cast<int8_t>((ws[e >> 2] >> (8 * (e & 3))) & 0xff));
+            const float x = static_cast<float>(static_cast<int>((ws[e >> 2] >> (8 * (e & 3))) & 0xff) - 128);
 #pragma unroll
             for (int h = 0; h < kMaxGroup; ++h)
               if (h < g) s[h] = fmaf(x, qs[h * D + ch * 16 + e], s[h]);
@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
         const float vsc = VS[uu];
         const int8_t* vr = V8 + static_cast<size_t>(uu) * D;
 #pragma unroll
-        for (int k = 0; k < DPL; ++k) v[k] = static_cast<float>(vr[lane + 32 * k]) * vsc;
+        for (int k = 0; k < DPL; ++k)
+          v[k] = static_cast<float>(static_cast<int>(static_cast<uint8_t>(vr[lane + 32 * k])) - 128) * vsc;
       } else {
         const __half* vr = V16 + static_cast<size_t>(uu - n8) * D;
 #pragma unroll

@@ -39,7 +39,6 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;
-constexpr uint32_t kBias = 0x80808080u;     // int8 -> biased uint8
 constexpr uint32_t kMagic = 0x64646464u;    // fp16 exponent byte of 1024
 constexpr uint32_t kH1152 = 0x64806480u;    // half2(1152, 1152)
 
@@ -101,16 +100,19 @@ __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
   return y;
 }
-// two biased int8 bytes of w (selected by sel) -> exact half2
+// two offset-binary code bytes of w (selected by sel) -> exact half2 of the codes
 __device__ __forceinline__ uint32_t i8h2(uint32_t w_biased, uint32_t sel) {
   uint32_t r = __byte_perm(w_biased, kMagic, sel);
   uint32_t m = kH1152;
   __half2 h = __hsub2(*reinterpret_cast<__half2*>(&r), *reinterpret_cast<__half2*>(&m));
   return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ uint32_t pack_h2(__half a, __half b) {
-  __half2 h = __halves2half2(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
+// x0, x1 -> fp16 pairs hi = (h0, h1) and lo = (x0 - h0, x1 - h1): hi + lo
+// carries x to ~2^-22 relative (x in fp16's normal range)
+__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(hi) : "f"(x1), "f"(x0));
+  const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(lo) : "f"(x1 - h.y), "f"(x0 - h.x));
 }
 __device__ __forceinline__ float gmax8(float v) {   // max over the 8 lanes sharing t4
   v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
@@ -263,6 +265,7 @@ __device__ __forceinline__ void issue_chunk(const Cache& c, int unit, int nc8, i
 
 struct SoftState {
   float mA, mB, lA, lB;   // queries 2*t4 (A) and 2*t4+1 (B)
+  float spA, spB;         // sum of P' over INT8 tokens (O's units), for the 1152 offset
   int E;                  // O holds values scaled by 2^E
 };
 
@@ -315,7 +318,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   float O[G::KS][4];
 #pragma unroll
   for (int mt = 0; mt < G::KS; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.0f;
-  SoftState ss{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
+  SoftState ss{-INFINITY, -INFINITY, 0.0f, 0.0f, 0.0f, 0.0f, 0};
   float* SC = c.scores + (static_cast<size_t>(lb) * c.Hq + kvh * g) * c.slots;
   const bool wA = 2 * t4 < g, wB = 2 * t4 + 1 < g;
 
@@ -329,6 +332,8 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     ss.lA *= cA;
     ss.lB *= cB;
     const float fA = cA * f, fB = cB * f;
+    ss.spA *= fA;
+    ss.spB *= fB;
 #pragma unroll
     for (int mt = 0; mt < G::KS; ++mt) {
       O[mt][0] *= fA;
@@ -343,33 +348,31 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   };
   // P' (4 values of the score layout) -> hi/lo B operands, then P'.V MMAs
   auto pv_int8 = [&](const float (&x)[4], const uint32_t (&vw)[4][G::VPT / 4]) {
-    const __half h0 = __float2half_rn(x[0]), h1 = __float2half_rn(x[1]);
-    const __half h2 = __float2half_rn(x[2]), h3 = __float2half_rn(x[3]);
-    const uint32_t bh0 = movtrans(pack_h2(h0, h1)), bh1 = movtrans(pack_h2(h2, h3));
-    const uint32_t bl0 = movtrans(pack_h2(__float2half_rn(x[0] - __half2float(h0)),
-                                          __float2half_rn(x[1] - __half2float(h1))));
-    const uint32_t bl1 = movtrans(pack_h2(__float2half_rn(x[2] - __half2float(h2)),
-                                          __float2half_rn(x[3] - __half2float(h3))));
+    uint32_t h01, l01, h23, l23;
+    split_pack(x[0], x[1], h01, l01);
+    split_pack(x[2], x[3], h23, l23);
+    const uint32_t bh0 = movtrans(h01), bh1 = movtrans(h23);
+    const uint32_t bl0 = movtrans(l01), bl1 = movtrans(l23);
 #pragma unroll
     for (int mt = 0; mt < G::KS; ++mt) {
       const int w = mt >> 1;
       const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-      const uint32_t p01 = __byte_perm(vw[0][w], vw[1][w], sel) ^ kBias;
-      const uint32_t p23 = __byte_perm(vw[2][w], vw[3][w], sel) ^ kBias;
-      const uint32_t a[4] = {i8h2(p01, 0x4140u), i8h2(p01, 0x4342u), i8h2(p23, 0x4140u),
-                             i8h2(p23, 0x4342u)};
+      // V^T operand as 1152 + code (exact in fp16); the 1152 * sum(P') term is
+      // removed once at the end
+      const uint32_t p01 = __byte_perm(vw[0][w], vw[1][w], sel);
+      const uint32_t p23 = __byte_perm(vw[2][w], vw[3][w], sel);
+      const uint32_t a[4] = {__byte_perm(p01, kMagic, 0x4140u), __byte_perm(p01, kMagic, 0x4342u),
+                             __byte_perm(p23, kMagic, 0x4140u), __byte_perm(p23, kMagic, 0x4342u)};
       mma16816(O[mt], a, bh0, bh1);
       mma16816(O[mt], a, bl0, bl1);
     }
   };
   auto pv_f16 = [&](const float (&x)[4], const uint32_t (&vw)[4][G::VPT / 2]) {
-    const __half h0 = __float2half_rn(x[0]), h1 = __float2half_rn(x[1]);
-    const __half h2 = __float2half_rn(x[2]), h3 = __float2half_rn(x[3]);
-    const uint32_t bh0 = movtrans(pack_h2(h0, h1)), bh1 = movtrans(pack_h2(h2, h3));
-    const uint32_t bl0 = movtrans(pack_h2(__float2half_rn(x[0] - __half2float(h0)),
-                                          __float2half_rn(x[1] - __half2float(h1))));
-    const uint32_t bl1 = movtrans(pack_h2(__float2half_rn(x[2] - __half2float(h2)),
-                                          __float2half_rn(x[3] - __half2float(h3))));
+    uint32_t h01, l01, h23, l23;
+    split_pack(x[0], x[1], h01, l01);
+    split_pack(x[2], x[3], h23, l23);
+    const uint32_t bh0 = movtrans(h01), bh1 = movtrans(h23);
+    const uint32_t bl0 = movtrans(l01), bl1 = movtrans(l23);
 #pragma unroll
     for (int mt = 0; mt < G::KS; ++mt) {
       const uint32_t a[4] = {__byte_perm(vw[0][mt], vw[1][mt], 0x5410u),
@@ -433,7 +436,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       for (int kk = 0; kk < G::KS; ++kk) {
 #pragma unroll
         for (int sb = 0; sb < 2; ++sb) {          // two independent accumulation chains
-          const uint32_t w0 = kw[sb][0][kk] ^ kBias, w1 = kw[sb][1][kk] ^ kBias;
+          const uint32_t w0 = kw[sb][0][kk], w1 = kw[sb][1][kk];
           const uint32_t a[4] = {i8h2(w0, 0x4140u), i8h2(w1, 0x4140u), i8h2(w0, 0x4342u),
                                  i8h2(w1, 0x4342u)};
           mma16816(s[sb], a, qb[kk][0], qb[kk][1]);
@@ -480,6 +483,8 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
         ss.lB += pB0 + pB1;
         const float vs0 = vsr[sb][0] * two, vs1 = vsr[sb][1] * two;
         const float x[4] = {pA0 * vs0, pB0 * vs0, pA1 * vs1, pB1 * vs1};
+        ss.spA += x[0] + x[2];
+        ss.spB += x[1] + x[3];
         uint32_t vw[4][G::VPT / 4];
 #pragma unroll
         for (int ii = 0; ii < 4; ++ii) {
@@ -583,6 +588,17 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   // ---- merge the warps of this CTA (shared memory reused) ----
   ss.lA = gsum8(ss.lA);
   ss.lB = gsum8(ss.lB);
+  {
+    // remove the 1152 * sum(P') the offset V operand added to every channel
+    const float oA = 1152.0f * gsum8(ss.spA), oB = 1152.0f * gsum8(ss.spB);
+#pragma unroll
+    for (int mt = 0; mt < G::KS; ++mt) {
+      O[mt][0] -= oA;
+      O[mt][2] -= oA;
+      O[mt][1] -= oB;
+      O[mt][3] -= oB;
+    }
+  }
   __syncthreads();
   float* wm = reinterpret_cast<float*>(smem);            // [kWarps][8]
   float* wl = wm + kWarps * 8;                           // [kWarps][8]

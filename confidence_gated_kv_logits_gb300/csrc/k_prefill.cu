@@ -36,7 +36,7 @@ k_prefill_store(Cache c, const __half* __restrict__ k, const __half* __restrict_
         for (int j = 0; j < per; ++j) {
           int q = 0;
           if (s != 0.0f) q = max(-127, min(127, __float2int_rn(__fdiv_rn(x[j], s))));
-          dst[lane * per + j] = static_cast<int8_t>(q);
+          dst[lane * per + j] = static_cast<int8_t>(q ^ 0x80);   // offset binary: code + 128
         }
         if (lane == 0) (isv ? c.vs : c.ks)[static_cast<size_t>(unit) * c.cap8 + i] = s;
       } else {

@@ -137,7 +137,7 @@ __device__ void quantize_row_warp(const __half* src, int8_t* dst, float* scale_o
       q = __float2int_rn(__fdiv_rn(x[j], s));
       q = max(-127, min(127, q));
     }
-    dst[lane * per + j] = static_cast<int8_t>(q);
+    dst[lane * per + j] = static_cast<int8_t>(q ^ 0x80);   // offset binary: code + 128
   }
   if (lane == 0) *scale_out = s;
 }
