@@ -57,6 +57,7 @@ struct confkv_ctx {
   float* part_ml = nullptr;
   float* part_acc = nullptr;
   unsigned int* ticket = nullptr;
+
   float* seed_out = nullptr;
   std::vector<void*> allocs;
   // staging of confkv_step_host
@@ -243,6 +244,7 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   A(dalloc(c, &c->part_ml, LB * c->Hq * c->splits * 2));
   A(dalloc(c, &c->part_acc, LB * c->Hq * c->splits * c->d));
   A(dalloc(c, &c->ticket, U));
+
   A(dalloc(c, &c->seed_out, LB * c->Hq * c->d));
   if (e == cudaSuccess) {
     std::vector<int32_t> bt(static_cast<size_t>(c->L) * 2);

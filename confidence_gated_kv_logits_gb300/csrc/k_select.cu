@@ -19,12 +19,15 @@
 // The fp32 operations use explicit _rn intrinsics so that no contraction
 // changes the rounding: the decision is taken in fp32 on exact fp32 values.
 //
-// One CTA of kThreads per (layer, sequence).  The same CTA then applies the
-// compaction: metadata and K/V data moves of every KV head, the INT8
-// quantisation of the aging token and the write of the new token.  Selection: the need-th largest
-// 64-bit key (key bits << 32 | position; unique) is found by an 8-bit MSB
-// radix select over the candidates (early exit once the boundary bucket is
-// taken whole); a single eviction, the steady state, is one arg-min.
+// One CTA of kThreads per (layer, sequence), small enough for every CTA of
+// the grid to be resident at once.  Keys stay in registers (kReg per thread).
+// Selection: the need-th largest 64-bit key (key bits << 32 | position;
+// unique) by an 8-bit MSB radix select over the candidates (early exit once
+// the boundary bucket is taken whole); a single eviction, the steady state,
+// is one arg-min.  Keep flags become 32-bit ballot masks; one warp per region
+// turns them into the compaction plan with popc / ffs.  The same CTA then
+// applies the compaction: metadata and K/V data moves of every KV head, the
+// INT8 quantisation of the aging token and the write of the new token.
 #include <cfloat>
 
 #include "confkv_internal.cuh"
@@ -32,76 +35,13 @@
 namespace confkv {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kReg = 4;        // slots per thread held in registers
+constexpr int kReg = 8;        // slots per thread held in registers (n <= 2048)
 
 __device__ __forceinline__ unsigned long long key64(float key, int pos) {
   return (static_cast<unsigned long long>(__float_as_uint(key)) << 32) |
          static_cast<unsigned int>(pos);
-}
-
-// Block-wide exclusive scan of two per-thread counts (ranks in thread order).
-__device__ __forceinline__ void block_scan2(int& a, int& b, int* wsum, int& tot_a, int& tot_b) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int ia = a, ib = b;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int xa = __shfl_up_sync(0xffffffffu, ia, o);
-    const int xb = __shfl_up_sync(0xffffffffu, ib, o);
-    if (lane >= o) { ia += xa; ib += xb; }
-  }
-  if (lane == 31) {
-    wsum[warp] = ia;
-    wsum[kWarps + warp] = ib;
-  }
-  __syncthreads();
-  int oa = 0, ob = 0, ta = 0, tb = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    const int xa = wsum[w], xb = wsum[kWarps + w];
-    if (w < warp) { oa += xa; ob += xb; }
-    ta += xa;
-    tb += xb;
-  }
-  a = oa + ia - a;
-  b = ob + ib - b;
-  tot_a = ta;
-  tot_b = tb;
-  __syncthreads();
-}
-
-// Plan of one dense region of n live slots that keeps nn of them: the slots
-// below nn that are not kept (holes) are filled, in rank order, by the kept
-// slots at or above nn (movers).  jobs[r].x = hole r, jobs[r].y = mover r.
-// Each thread scans 8 consecutive slots per pass.  Returns the mover count.
-__device__ int plan_region(const unsigned char* f, int n, int nn, int2* jobs, int* wsum) {
-  constexpr int kPer = 8;
-  const int lim = max(n, nn);
-  int hbase = 0, mbase = 0;
-  for (int base = 0; base < lim; base += kThreads * kPer) {
-    const int j0 = base + threadIdx.x * kPer;
-    int hc = 0, mc = 0;
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      const int j = j0 + e;
-      if (j < nn) hc += (j >= n || !f[j]) ? 1 : 0;
-      else if (j < n) mc += f[j] ? 1 : 0;
-    }
-    int th, tm;
-    block_scan2(hc, mc, wsum, th, tm);
-    int rh = hbase + hc, rm = mbase + mc;
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      const int j = j0 + e;
-      if (j < nn) {
-        if (j >= n || !f[j]) jobs[rh++].x = j;
-      } else if (j < n && f[j]) {
-        jobs[rm++].y = j;
-      }
-    }
-    hbase += th;
-    mbase += tm;
-  }
-  return mbase;
 }
 
 __device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v,
@@ -117,6 +57,62 @@ __device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v
   for (int w = 1; w < kWarps; ++w) r = sh[w] < r ? sh[w] : r;
   __syncthreads();
   return r;
+}
+
+// bits [0, k) set (k clamped to [0, 32])
+__device__ __forceinline__ unsigned lowmask(int k) {
+  return k >= 32 ? 0xffffffffu : (k <= 0 ? 0u : ((1u << k) - 1u));
+}
+
+// Compaction plan of one dense region, by one warp.  bits: word q holds the
+// keep flags of slots [32q, 32q + 32) (bits at or beyond n are ignored).
+// The region keeps kc + extra slots (extra: tokens that arrive in it);
+// holes = slots below min(n, nn) not kept, then slot n when nn > n;
+// movers = kept slots in [nn, n).  jobs[r].x = hole r, jobs[r].y = mover r,
+// both in slot order.  Returns the mover count; *nn_out = nn.
+__device__ int plan_warp(const unsigned* bits, int n, int extra, int2* jobs, int* nn_out) {
+  const int lane = threadIdx.x & 31;
+  const int nw = (n + 31) >> 5;
+  const int per = (nw + 31) >> 5;
+  const int w0 = min(nw, lane * per), w1 = min(nw, w0 + per);
+  int kc = 0;
+  for (int q = w0; q < w1; ++q) kc += __popc(bits[q] & lowmask(n - 32 * q));
+  for (int o = 16; o > 0; o >>= 1) kc += __shfl_xor_sync(0xffffffffu, kc, o);
+  const int nn = kc + extra;
+  const int hl = min(n, nn);
+  int hc = 0, mc = 0;
+  for (int q = w0; q < w1; ++q) {
+    const unsigned kb = bits[q];
+    hc += __popc(~kb & lowmask(hl - 32 * q));
+    mc += __popc(kb & lowmask(n - 32 * q) & ~lowmask(nn - 32 * q));
+  }
+  int hs = hc, ms = mc;                     // inclusive scans over lanes
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, hs, o);
+    const int y = __shfl_up_sync(0xffffffffu, ms, o);
+    if (lane >= o) { hs += x; ms += y; }
+  }
+  const int htot = __shfl_sync(0xffffffffu, hs, 31), mtot = __shfl_sync(0xffffffffu, ms, 31);
+  hs -= hc;
+  ms -= mc;
+  for (int q = w0; q < w1; ++q) {
+    const unsigned kb = bits[q];
+    unsigned hm = ~kb & lowmask(hl - 32 * q);
+    unsigned mm = kb & lowmask(n - 32 * q) & ~lowmask(nn - 32 * q);
+    while (hm) {
+      const int bit = __ffs(hm) - 1;
+      jobs[hs++].x = 32 * q + bit;
+      hm &= hm - 1u;
+    }
+    while (mm) {
+      const int bit = __ffs(mm) - 1;
+      jobs[ms++].y = 32 * q + bit;
+      mm &= mm - 1u;
+    }
+  }
+  if (nn > n && lane == 0) jobs[htot].x = n;  // the arriving token's slot past the end
+  *nn_out = nn;
+  return mtot;
 }
 
 // warp-level INT8 absmax quantisation of one fp16 row of d elements
@@ -142,92 +138,103 @@ __device__ void quantize_row_warp(const __half* src, int8_t* dst, float* scale_o
   if (lane == 0) *scale_out = s;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) k_select(Cache c, StepParams sp) {
+__global__ void __launch_bounds__(kThreads, 4) k_select(Cache c, StepParams sp) {
   const int lb = blockIdx.x;
   const int l = lb / c.B, b = lb % c.B;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n8 = c.n8[lb], n16 = c.n16[lb];
   const int N = sp.btab[l * 2 + (sp.hi[b] ? 1 : 0)];
   const int t = sp.t;
-  const int Hkv = c.Hkv, cap8 = c.cap8, W = c.W, P = c.P;
-  const size_t lbs = static_cast<size_t>(lb) * c.slots;
+  const int Hkv = c.Hkv, cap8 = c.cap8, W = c.W, P = c.P, d = c.d;
   int32_t* pos8 = c.pos8 + static_cast<size_t>(lb) * cap8;
   int32_t* pos16 = c.pos16 + static_cast<size_t>(lb) * c.Wr;
   float* ema8 = c.ema8 + static_cast<size_t>(lb) * cap8;
   float* ema16 = c.ema16 + static_cast<size_t>(lb) * c.Wr;
-  float* keys = c.keys + lbs;
+  float* keys = c.keys + static_cast<size_t>(lb) * c.slots;
   const float* mass = c.mass + static_cast<size_t>(lb) * Hkv * c.slots;
 
-  __shared__ int s_prot, s_jage, s_D, s_k, s_cnt;
+  // dynamic shared memory: unified keep mask | FP16 keep mask | INT8 jobs | FP16 jobs
+  extern __shared__ __align__(16) unsigned char dsm[];
+  const int uwords = (cap8 + c.Wr) / 32 + 2;
+  const int fwords = c.Wr / 32 + 2;
+  unsigned* ubits = reinterpret_cast<unsigned*>(dsm);
+  unsigned* fbits = ubits + uwords;
+  int2* sj8 = reinterpret_cast<int2*>(dsm + ((static_cast<size_t>(uwords + fwords) * 4 + 15) & ~static_cast<size_t>(15)));
+  int2* sj16 = sj8 + c.Ncap + 1;
+
+  __shared__ int s_prot, s_jage, s_D, s_k, s_cnt, s_keptA, s_nn8, s_nn16, s_mov8, s_mov16;
   __shared__ int s_hist[256];
-  __shared__ int s_wsum[2 * kWarps];
   __shared__ unsigned long long s_min[kWarps];
-  if (tid == 0) { s_prot = 0; s_jage = -1; }
+  if (tid == 0) { s_prot = 0; s_jage = -1; s_keptA = 0; }
   __syncthreads();
 
   // ---- phase A: EMA update and ranking keys of every cached token.
-  // Slots are taken kReg per thread per round with all loads issued first;
-  // when n <= kReg * kThreads the 64-bit keys stay in registers for the
-  // selection and the flag pass (otherwise they are re-read from `keys`).
+  // Slot i (unified order: INT8 slots, then FP16 slots) of round `base` is
+  // base + r * kThreads + tid; all loads of a half-round are issued first.
   const int ntok = n8 + n16;
   const bool in_regs = ntok <= kReg * kThreads;
   unsigned long long rkey[kReg];
-  bool rcand[kReg];
+  unsigned rcand = 0;                       // bit r: slot of register r is a candidate
   unsigned long long lmin = ~0ull;
   int lprot = 0;
   const float hqf = static_cast<float>(c.Hq);
-  for (int base = 0; base < ntok; base += kReg * kThreads) {
-    int sid[kReg], pv[kReg];
-    float ev[kReg], asum[kReg];
+for (int base = 0; base < ntok; base += kReg * kThreads) {
 #pragma unroll
-    for (int r = 0; r < kReg; ++r) {
-      const int i = base + r * kThreads + tid;
-      const bool is8 = i < n8;
-      const int j = is8 ? i : i - n8;
-      sid[r] = (i < ntok) ? (is8 ? j : cap8 + j) : -1;
-      pv[r] = (i < ntok) ? (is8 ? pos8[j] : pos16[j]) : 0;
-      ev[r] = (i < ntok) ? (is8 ? ema8[j] : ema16[j]) : 0.0f;
-      asum[r] = 0.0f;
-    }
-    for (int h = 0; h < Hkv; ++h) {
-      const float* mh = mass + static_cast<size_t>(h) * c.slots;
+    for (int half = 0; half < 2; ++half) {
+      constexpr int kH = kReg / 2;
+      int sid[kH], pv[kH];
+      float ev[kH], asum[kH];
 #pragma unroll
-      for (int r = 0; r < kReg; ++r)
-        if (sid[r] >= 0) asum[r] = __fadd_rn(asum[r], mh[sid[r]]);
-    }
+      for (int r = 0; r < kH; ++r) {
+        const int i = base + (half * kH + r) * kThreads + tid;
+        const bool is8 = i < n8;
+        const int j = is8 ? i : i - n8;
+        sid[r] = (i < ntok) ? (is8 ? j : cap8 + j) : -1;
+        pv[r] = (i < ntok) ? (is8 ? pos8[j] : pos16[j]) : 0;
+        ev[r] = (i < ntok) ? (is8 ? ema8[j] : ema16[j]) : 0.0f;
+        asum[r] = 0.0f;
+      }
+      for (int h = 0; h < Hkv; ++h) {
+        const float* mh = mass + static_cast<size_t>(h) * c.slots;
 #pragma unroll
-    for (int r = 0; r < kReg; ++r) {
-      rcand[r] = false;
-      if (sid[r] < 0) continue;
-      const int i = base + r * kThreads + tid;
-      const bool is8 = i < n8;
-      const int j = is8 ? i : i - n8;
-      const float a = __fdiv_rn(asum[r], hqf);
-      const float e = __fadd_rn(__fmul_rn(sp.beta, ev[r]), __fmul_rn(sp.omb, a));
-      if (is8) ema8[j] = e; else ema16[j] = e;
-      const int age = t - pv[r];
-      const float key = __fadd_rn(e, __fdiv_rn(1.0f, static_cast<float>(1 + age)));
-      keys[sid[r]] = key;
-      const bool prot = !is8 && age < P;
-      if (prot) ++lprot;
-      if (!is8 && age == W) s_jage = j;
-      const unsigned long long k64 = key64(key, pv[r]);
-      rkey[r] = k64;
-      rcand[r] = !prot;
-      if (!prot) lmin = k64 < lmin ? k64 : lmin;
+        for (int r = 0; r < kH; ++r)
+          if (sid[r] >= 0) asum[r] = __fadd_rn(asum[r], mh[sid[r]]);
+      }
+#pragma unroll
+      for (int r = 0; r < kH; ++r) {
+        const int rr = half * kH + r;
+        if (sid[r] < 0) { rkey[rr] = 0; continue; }
+        const int i = base + rr * kThreads + tid;
+        const bool is8 = i < n8;
+        const int j = is8 ? i : i - n8;
+        const float a = __fdiv_rn(asum[r], hqf);
+        const float e = __fadd_rn(__fmul_rn(sp.beta, ev[r]), __fmul_rn(sp.omb, a));
+        if (is8) ema8[j] = e; else ema16[j] = e;
+        const int age = t - pv[r];
+        const float key = __fadd_rn(e, __fdiv_rn(1.0f, static_cast<float>(1 + age)));
+        keys[sid[r]] = key;
+        const bool prot = !is8 && age < P;
+        if (prot) ++lprot;
+        if (!is8 && age == W) s_jage = j;
+        const unsigned long long k64 = key64(key, pv[r]);
+        rkey[rr] = k64;
+        if (!prot) {
+          rcand |= 1u << rr;
+          lmin = k64 < lmin ? k64 : lmin;
+        }
+      }
     }
   }
   for (int o = 16; o > 0; o >>= 1) lprot += __shfl_xor_sync(0xffffffffu, lprot, o);
-  if ((tid & 31) == 0 && lprot) atomicAdd(&s_prot, lprot);
+  if (lane == 0 && lprot) atomicAdd(&s_prot, lprot);
   __syncthreads();
   const int pcount = s_prot + 1;            // + the new token
   const int jage = s_jage;
-  const int n_tot = n8 + n16 + 1;
+  const int n_tot = ntok + 1;
   // keep rule for candidates: mode 0 keep all, 1 keep none,
   // 2 (key & mask) >= prefix, 3 key != kmin (exactly one eviction)
   int mode = 0;
   unsigned long long mask = 0, prefix = 0, kmin = 0;
-  // candidate key of slot i (unified order), or false if protected
   auto cand_key = [&](int i, unsigned long long& k64) -> bool {
     const bool is8 = i < n8;
     const int j = is8 ? i : i - n8;
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_select(Cache c, StepParams sp) 
         if (in_regs) {
 #pragma unroll
           for (int r = 0; r < kReg; ++r)
-            if (rcand[r] && (rkey[r] & mask) == prefix)
+            if (((rcand >> r) & 1u) && (rkey[r] & mask) == prefix)
               atomicAdd(&s_hist[(rkey[r] >> shift) & 255u], 1);
         } else {
           for (int i = tid; i < ntok; i += kThreads) {
@@ -298,102 +305,108 @@ __global__ void __launch_bounds__(kThreads, 2) k_select(Cache c, StepParams sp) 
     return kk != kmin;
   };
 
-  // ---- keep flags in shared memory: one pass over the slots ----
-  // fl8[j]: INT8 slot j kept; fl16[j]: FP16 slot j kept and staying FP16
-  extern __shared__ __align__(16) unsigned char fl[];
-  unsigned char* fl8 = fl;
-  unsigned char* fl16 = fl + cap8;
-  int2* sj8 = reinterpret_cast<int2*>(fl + ((cap8 + c.Wr + 15) & ~15));   // [Ncap + 1]
-  int2* sj16 = sj8 + c.Ncap + 1;                                            // [Wr]
-  __shared__ int s_k8, s_k16, s_keptA;
-  if (tid == 0) {
-    s_k8 = 0;
-    s_k16 = 0;
-    s_keptA = 0;
-  }
-  __syncthreads();
+  // ---- keep masks: bit i of ubits = unified slot i kept (and, for the FP16
+  // region, staying FP16: the aging token's bit is cleared) ----
   {
-    int c8 = 0, c16 = 0;
-    auto flag = [&](int i, bool cand, unsigned long long kk) {
-      const bool k = !cand || keep_key(kk);
-      if (i < n8) {
-        fl8[i] = k;
-        c8 += k;
-      } else {
-        const int j = i - n8;
-        if (j == jage) {
+    auto put = [&](int rr, int i, bool cand, unsigned long long kk) {
+      bool k = false;
+      if (i < ntok) {
+        k = !cand || keep_key(kk);
+        if (i >= n8 && i - n8 == jage) {
           s_keptA = k;
-          fl16[j] = 0;
-        } else {
-          fl16[j] = k;
-          c16 += k;
+          k = false;
         }
       }
+      const unsigned m = __ballot_sync(0xffffffffu, k);
+      if (lane == 0) ubits[rr * kWarps + warp] = m;
     };
     if (in_regs) {
 #pragma unroll
-      for (int r = 0; r < kReg; ++r) {
-        const int i = r * kThreads + tid;
-        if (i < ntok) flag(i, rcand[r], rkey[r]);
+      for (int rr = 0; rr < kReg; ++rr) {
+        const int i = rr * kThreads + tid;
+        if (rr * kThreads < ntok) put(rr, i, (rcand >> rr) & 1u, rkey[rr]);
       }
     } else {
-      for (int i = tid; i < ntok; i += kThreads) {
+      const int rounds = (ntok + kThreads - 1) / kThreads;
+      for (int rr = 0; rr < rounds; ++rr) {
+        const int i = rr * kThreads + tid;
         unsigned long long kk = 0;
-        const bool cand = cand_key(i, kk);
-        flag(i, cand, kk);
+        const bool cand = (i < ntok) ? cand_key(i, kk) : false;
+        put(rr, i, cand, kk);
       }
     }
-    for (int o = 16; o > 0; o >>= 1) {
-      c8 += __shfl_xor_sync(0xffffffffu, c8, o);
-      c16 += __shfl_xor_sync(0xffffffffu, c16, o);
-    }
-    if ((tid & 31) == 0) {
-      atomicAdd(&s_k8, c8);
-      atomicAdd(&s_k16, c16);
-    }
+    const int nw = (ntok + 31) / 32;
+    for (int q = nw + tid; q < uwords; q += kThreads) ubits[q] = 0u;
+  }
+  __syncthreads();
+  // FP16 keep mask: unified bits [n8, n8 + n16) shifted down to slot 0
+  for (int q = tid; q < (n16 + 31) / 32; q += kThreads) {
+    const int bit0 = n8 + 32 * q;
+    fbits[q] = __funnelshift_r(ubits[bit0 >> 5], ubits[(bit0 >> 5) + 1], bit0 & 31);
   }
   __syncthreads();
   const bool keptA = s_keptA != 0;
-  const int n8n = s_k8 + (keptA ? 1 : 0);
-  const int n16n = s_k16 + 1;
-  // ---- compaction plans: hole of rank r <- mover of rank r ----
-  const int nmov8 = plan_region(fl8, n8, n8n, sj8, s_wsum);
-  const int nmov16 = plan_region(fl16, n16, n16n, sj16, s_wsum);
-  if (tid == 0) sj16[nmov16].y = -1;        // the new token fills the last FP16 hole
+  // ---- compaction plans: warp 0 the INT8 region, warp 1 the FP16 region ----
+  if (warp == 0) {
+    int nn;
+    const int mv = plan_warp(ubits, n8, keptA ? 1 : 0, sj8, &nn);
+    if (lane == 0) { s_nn8 = nn; s_mov8 = mv; }
+  } else if (warp == 1) {
+    int nn;
+    const int mv = plan_warp(fbits, n16, 1, sj16, &nn);
+    if (lane == 0) {
+      s_nn16 = nn;
+      s_mov16 = mv;
+      sj16[mv].y = -1;                      // the new token fills the last FP16 hole
+    }
+  }
   __syncthreads();
+  const int n8n = s_nn8, n16n = s_nn16, nmov8 = s_mov8, nmov16 = s_mov16;
 
-  // ---- phase C: data and metadata moves.  INT8 destinations first: the
-  // aging token is read from its FP16 slot before FP16 slots are rewritten ----
-  const int2* j8 = sj8;
-  const int2* j16 = sj16;
-  const int d = c.d;
-  const int warp = tid >> 5, lane = tid & 31;
+  // ---- data and metadata moves.  INT8 destinations first: the aging token
+  // is read from its FP16 slot before FP16 slots are rewritten ----
   {
-    // one warp per (move, KV head): lanes copy the 16-byte pieces of the K and
-    // V rows, two more lanes the two scales
-    const int cpr = d / 16;
-    for (int p = warp; p < nmov8 * Hkv; p += kWarps) {
-      const int r = p / Hkv, h = p - r * Hkv;
-      const int2 jb = j8[r];
-      const size_t u8 = (static_cast<size_t>(lb) * Hkv + h) * cap8;
-      if (lane < 2 * cpr) {
-        int8_t* base = (lane < cpr ? c.k8 : c.v8) + u8 * d;
-        const int ch = lane < cpr ? lane : lane - cpr;
-        reinterpret_cast<int4*>(base + static_cast<size_t>(jb.x) * d)[ch] =
-            reinterpret_cast<const int4*>(base + static_cast<size_t>(jb.y) * d)[ch];
-      } else if (lane < 2 * cpr + 2) {
-        float* sc = (lane == 2 * cpr) ? c.ks : c.vs;
-        sc[u8 + jb.x] = sc[u8 + jb.y];
+    // INT8 moves: every (move, KV head, 16-byte piece of K or V) is one item;
+    // each thread loads 4 items before storing them (4 loads in flight)
+    const int cpr = d / 16, per = 2 * cpr, items = nmov8 * Hkv * per;
+    for (int base = 0; base < items; base += 4 * kThreads) {
+      int4 v[4];
+      int8_t* dst[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int it = base + u * kThreads + tid;
+        dst[u] = nullptr;
+        if (it < items) {
+          const int r = it / (Hkv * per);
+          const int rem = it - r * Hkv * per;
+          const int h = rem / per, pc = rem - h * per;
+          const int2 jb = sj8[r];
+          int8_t* rows = (pc < cpr ? c.k8 : c.v8) + (static_cast<size_t>(lb) * Hkv + h) * cap8 * d;
+          const int ch = pc < cpr ? pc : pc - cpr;
+          v[u] = reinterpret_cast<const int4*>(rows + static_cast<size_t>(jb.y) * d)[ch];
+          dst[u] = rows + static_cast<size_t>(jb.x) * d + 16 * ch;
+        }
       }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (dst[u]) *reinterpret_cast<int4*>(dst[u]) = v[u];
+    }
+    for (int it = tid; it < nmov8 * Hkv; it += kThreads) {
+      const int r = it / Hkv, h = it - r * Hkv;
+      const int2 jb = sj8[r];
+      const size_t u8 = (static_cast<size_t>(lb) * Hkv + h) * cap8;
+      const float ksv = c.ks[u8 + jb.y], vsv = c.vs[u8 + jb.y];
+      c.ks[u8 + jb.x] = ksv;
+      c.vs[u8 + jb.x] = vsv;
     }
   }
   for (int r = tid; r < nmov8; r += kThreads) {
-    const int2 jb = j8[r];
+    const int2 jb = sj8[r];
     pos8[jb.x] = pos8[jb.y];
     ema8[jb.x] = ema8[jb.y];
   }
   if (keptA) {
-    const int hage = j8[nmov8].x;
+    const int hage = sj8[nmov8].x;
     if (tid == 0) {
       pos8[hage] = pos16[jage];
       ema8[hage] = ema16[jage];
@@ -411,30 +424,43 @@ __global__ void __launch_bounds__(kThreads, 2) k_select(Cache c, StepParams sp) 
   }
   __syncthreads();
   {
-    // one warp per (FP16 move or new token, KV head): one lane per 16-byte piece
-    const int cpr = d / 8;
-    for (int p = warp; p < (nmov16 + 1) * Hkv; p += kWarps) {
-      const int r = p / Hkv, h = p - r * Hkv;
-      if (lane < 2 * cpr) {
-        const int2 jb = j16[r];
-        const size_t u8 = static_cast<size_t>(lb) * Hkv + h;
-        const bool isv = lane >= cpr;
-        const int ch = isv ? lane - cpr : lane;
-        __half* base = (isv ? c.v16 : c.k16) + u8 * c.Wr * d;
-        const __half* src = (jb.y >= 0) ? base + static_cast<size_t>(jb.y) * d
-                                        : (isv ? sp.v_new : sp.k_new) + u8 * d;
-        reinterpret_cast<int4*>(base + static_cast<size_t>(jb.x) * d)[ch] =
-            reinterpret_cast<const int4*>(src)[ch];
+    // FP16 moves and the new token: (move, KV head, 16-byte piece) items,
+    // 4 loads in flight per thread
+    const int cpr = d / 8, per = 2 * cpr, items = (nmov16 + 1) * Hkv * per;
+    for (int base = 0; base < items; base += 4 * kThreads) {
+      int4 v[4];
+      __half* dst[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int it = base + u * kThreads + tid;
+        dst[u] = nullptr;
+        if (it < items) {
+          const int r = it / (Hkv * per);
+          const int rem = it - r * Hkv * per;
+          const int h = rem / per, pc = rem - h * per;
+          const int2 jb = sj16[r];
+          const size_t u8 = static_cast<size_t>(lb) * Hkv + h;
+          const bool isv = pc >= cpr;
+          const int ch = isv ? pc - cpr : pc;
+          __half* rows = (isv ? c.v16 : c.k16) + u8 * c.Wr * d;
+          const __half* src = (jb.y >= 0) ? rows + static_cast<size_t>(jb.y) * d
+                                          : (isv ? sp.v_new : sp.k_new) + u8 * d;
+          v[u] = reinterpret_cast<const int4*>(src)[ch];
+          dst[u] = rows + static_cast<size_t>(jb.x) * d + 8 * ch;
+        }
       }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (dst[u]) *reinterpret_cast<int4*>(dst[u]) = v[u];
     }
   }
   for (int r = tid; r < nmov16; r += kThreads) {
-    const int2 jb = j16[r];
+    const int2 jb = sj16[r];
     pos16[jb.x] = pos16[jb.y];
     ema16[jb.x] = ema16[jb.y];
   }
   if (tid == 0) {
-    const int hn = j16[nmov16].x;
+    const int hn = sj16[nmov16].x;
     pos16[hn] = t;
     ema16[hn] = 0.0f;
   }
@@ -466,16 +492,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_select(Cache c, StepParams sp) 
     atomicAdd(&c.stats->moved, static_cast<unsigned long long>(nmov8 + nmov16));
     atomicAdd(&c.stats->kv_bytes,
               static_cast<unsigned long long>(Hkv) *
-                  (static_cast<unsigned long long>(n8n) * (2ull * c.d + 8ull) +
-                   static_cast<unsigned long long>(n16n) * 4ull * c.d));
+                  (static_cast<unsigned long long>(n8n) * (2ull * d + 8ull) +
+                   static_cast<unsigned long long>(n16n) * 4ull * d));
   }
 }
 
 }  // namespace
 
+size_t select_smem_bytes(const Cache& c) {
+  const size_t uwords = (static_cast<size_t>(c.cap8) + c.Wr) / 32 + 2;
+  const size_t fwords = static_cast<size_t>(c.Wr) / 32 + 2;
+  return (((uwords + fwords) * 4 + 15) & ~static_cast<size_t>(15)) +
+         (static_cast<size_t>(c.Ncap) + 1 + c.Wr) * sizeof(int2);
+}
+
 cudaError_t launch_select(const Cache& c, const StepParams& sp, cudaStream_t s) {
-  const size_t smem = ((static_cast<size_t>(c.cap8) + c.Wr + 15) & ~static_cast<size_t>(15)) +
-                      (static_cast<size_t>(c.Ncap) + 1 + c.Wr) * sizeof(int2);
+  const size_t smem = select_smem_bytes(c);
   static size_t attr = 48 * 1024;
   if (smem > attr) {
     const cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
