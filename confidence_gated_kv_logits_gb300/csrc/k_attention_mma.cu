@@ -281,22 +281,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
   const int unit = blockIdx.x, split = blockIdx.y;
   const int lb = unit / c.Hkv, kvh = unit - lb * c.Hkv, g = c.g;
-  const int n8 = c.n8[lb], n16 = c.n16[lb];
-  const int nc8 = (n8 + 31) >> 5, nc16 = (n16 + 15) >> 4, nc = nc8 + nc16;
-  const int cb = static_cast<int>(static_cast<long long>(nc) * split / ap.splits);
-  const int ce = static_cast<int>(static_cast<long long>(nc) * (split + 1) / ap.splits);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, t4 = lane & 3;
-  const int cnt = (ce - cb > warp) ? (ce - cb - warp + kWarps - 1) / kWarps : 0;
-  const uint32_t wbase = smem_u32(smem) + warp * kStages * STAGE;
-  if constexpr (TMA) {
-    if (lane == 0)
-      for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    __syncwarp();
-  }
-  bool ok_all = true;
-  int fail_i = 0;
-
   // Q^T operand: query gid, channels t4*KPT + 4kk + {0,1} and {2,3}
   uint32_t qb[G::KS][2];
   if (gid < g) {
@@ -314,6 +299,23 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
 #pragma unroll
     for (int kk = 0; kk < G::KS; ++kk) qb[kk][0] = qb[kk][1] = 0u;
   }
+
+  // everything below reads the selection kernel's results
+  pdl_wait();
+  const int n8 = c.n8[lb], n16 = c.n16[lb];
+  const int nc8 = (n8 + 31) >> 5, nc16 = (n16 + 15) >> 4, nc = nc8 + nc16;
+  const int cb = static_cast<int>(static_cast<long long>(nc) * split / ap.splits);
+  const int ce = static_cast<int>(static_cast<long long>(nc) * (split + 1) / ap.splits);
+  const int cnt = (ce - cb > warp) ? (ce - cb - warp + kWarps - 1) / kWarps : 0;
+  const uint32_t wbase = smem_u32(smem) + warp * kStages * STAGE;
+  if constexpr (TMA) {
+    if (lane == 0)
+      for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    __syncwarp();
+  }
+  bool ok_all = true;
+  int fail_i = 0;
 
   float O[G::KS][4];
 #pragma unroll
@@ -577,6 +579,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     }
   }
   if constexpr (!TMA) cp_wait<0>();
+  pdl_trigger();     // the next kernel in the stream may be scheduled
   if (!ok_all) {
     // a tile never arrived: flag the step (its output for this unit is
     // incomplete) and give the copy in flight one more bounded wait before
@@ -711,8 +714,9 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k_attn_mma<D, TMA><<<dim3(c.L * c.B * c.Hkv, ap.splits), kThreads, smem, s>>>(c, ap, tm);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(k_attn_mma<D, TMA>, dim3(c.L * c.B * c.Hkv, ap.splits),
+                                   dim3(kThreads), smem, s, c, ap, tm);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

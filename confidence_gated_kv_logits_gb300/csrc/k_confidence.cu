@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kThreads)
 k_confidence(const float* __restrict__ logits, int V, int cps, float tau, int N_low, int N_high,
              float* conf, int32_t* hi, float* conf_out, int32_t* budget_out, int32_t* err,
              DevStats* st, ConfPart* part, unsigned int* ticket) {
+  pdl_wait();        // the logits (and the previous step) are complete
+  pdl_trigger();     // the selection may start its EMA pass meanwhile
   const int b = blockIdx.x / cps;
   const int rk = blockIdx.x - b * cps;
   const long long lo = static_cast<long long>(V) * rk / cps;
@@ -179,9 +181,10 @@ cudaError_t launch_confidence(const float* logits, int B, int V, float tau, int 
                               int32_t* budget_out, int32_t* err, DevStats* st, ConfPart* part,
                               unsigned int* ticket, cudaStream_t s) {
   const int cps = confidence_ctas_per_seq(B, V);
-  k_confidence<<<B * cps, kThreads, 0, s>>>(logits, V, cps, tau, N_low, N_high, conf, hi,
-                                            conf_out, budget_out, err, st, part, ticket);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(k_confidence, dim3(B * cps), dim3(kThreads), 0, s, logits, V,
+                                   cps, tau, N_low, N_high, conf, hi, conf_out, budget_out, err,
+                                   st, part, ticket);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------

@@ -142,8 +142,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_select(Cache c, StepParams sp) 
   const int lb = blockIdx.x;
   const int l = lb / c.B, b = lb % c.B;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();     // the attention may be scheduled (it waits for this grid)
+  // n8, n16, positions, EMA and mass come from the previous step, which the
+  // confidence kernel has already waited for; the budget is read after
+  // pdl_wait() below
   const int n8 = c.n8[lb], n16 = c.n16[lb];
-  const int N = sp.btab[l * 2 + (sp.hi[b] ? 1 : 0)];
   const int t = sp.t;
   const int Hkv = c.Hkv, cap8 = c.cap8, W = c.W, P = c.P, d = c.d;
   int32_t* pos8 = c.pos8 + static_cast<size_t>(lb) * cap8;
@@ -227,6 +230,8 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
   }
   for (int o = 16; o > 0; o >>= 1) lprot += __shfl_xor_sync(0xffffffffu, lprot, o);
   if (lane == 0 && lprot) atomicAdd(&s_prot, lprot);
+  pdl_wait();        // the confidence kernel's budget flags are complete
+  const int N = sp.btab[l * 2 + (sp.hi[b] ? 1 : 0)];
   __syncthreads();
   const int pcount = s_prot + 1;            // + the new token
   const int jage = s_jage;
@@ -515,8 +520,8 @@ cudaError_t launch_select(const Cache& c, const StepParams& sp, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     attr = smem;
   }
-  k_select<<<c.L * c.B, kThreads, smem, s>>>(c, sp);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(k_select, dim3(c.L * c.B), dim3(kThreads), smem, s, c, sp);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace confkv
