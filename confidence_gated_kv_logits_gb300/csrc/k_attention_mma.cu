@@ -165,12 +165,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, unsigned parity) {
     if (mbar_try(bar, parity)) return true;
   return false;
 }
+// L2 policy for the streamed K/V tiles: evict first, so that the scores and
+// masses this kernel writes and re-reads stay resident
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                       uint32_t bar) {
+                                       uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void bulk_1d(uint32_t dst, const void* src, unsigned bytes, uint32_t bar) {
@@ -193,20 +200,21 @@ struct TmaMaps {
 // x 256 B as two 128-byte-wide boxes each.
 __device__ __forceinline__ void issue_chunk_tma(const Cache& c, const TmaMaps& tm, int unit,
                                                 int nc8, int ci, uint32_t st, uint32_t bar) {
+  const uint64_t pol = evict_first_policy();
   if (ci < nc8) {
     const int row0 = unit * c.cap8 + 32 * ci;
     mbar_expect_tx(bar, 2 * 4096 + 256);
-    tma_2d(st, &tm.k8, 0, row0, bar);
-    tma_2d(st + 4096, &tm.v8, 0, row0, bar);
+    tma_2d(st, &tm.k8, 0, row0, bar, pol);
+    tma_2d(st + 4096, &tm.v8, 0, row0, bar, pol);
     bulk_1d(st + 8192, c.ks + row0, 128, bar);
     bulk_1d(st + 8192 + 128, c.vs + row0, 128, bar);
   } else {
     const int row0 = unit * c.Wr + 16 * (ci - nc8);
     mbar_expect_tx(bar, 2 * 4096);
-    tma_2d(st, &tm.k16, 0, row0, bar);
-    tma_2d(st + 2048, &tm.k16, 64, row0, bar);
-    tma_2d(st + 4096, &tm.v16, 0, row0, bar);
-    tma_2d(st + 6144, &tm.v16, 64, row0, bar);
+    tma_2d(st, &tm.k16, 0, row0, bar, pol);
+    tma_2d(st + 2048, &tm.k16, 64, row0, bar, pol);
+    tma_2d(st + 4096, &tm.v16, 0, row0, bar, pol);
+    tma_2d(st + 6144, &tm.v16, 64, row0, bar, pol);
   }
 }
 
