@@ -32,7 +32,7 @@ FLAG_TIMEOUT = 4
 EXPORTS = ("confkv_create", "confkv_prefill", "confkv_step", "confkv_step_host",
            "confkv_stats", "confkv_read_cache", "confkv_profile_enable",
            "confkv_profile_read", "confkv_last_error", "confkv_free",
-           "confkv_confidence_noalloc")
+           "confkv_confidence_noalloc", "confkv_step_begin", "confkv_step_layer")
 
 
 class ConfKVError(RuntimeError):
@@ -85,6 +85,10 @@ def load_library(path=LIB_PATH):
     L.confkv_prefill.argtypes = [vp, vp, vp, ci, vp, vp]
     L.confkv_step.restype = ci
     L.confkv_step.argtypes = [vp] * 11
+    L.confkv_step_begin.restype = ci
+    L.confkv_step_begin.argtypes = [vp] * 5
+    L.confkv_step_layer.restype = ci
+    L.confkv_step_layer.argtypes = [vp, ci] + [vp] * 7
     L.confkv_step_host.restype = ci
     L.confkv_step_host.argtypes = [vp] * 11
     L.confkv_stats.restype = ci
@@ -198,6 +202,26 @@ class ConfKV:
                 _dptr(conf, torch.float32, B, "conf", dev),
                 _dptr(budget, torch.int32, B, "budget", dev)]
         self._check(self._L.confkv_step(self._h, *args, self._stream(stream)))
+
+    def step_begin(self, logits, conf=None, budget=None, stream=None):
+        import torch
+        B, dev = self.B, self.device
+        self._check(self._L.confkv_step_begin(
+            self._h, _dptr(logits, torch.float32, B * self.V, "logits", dev),
+            _dptr(conf, torch.float32, B, "conf", dev), _dptr(budget, torch.int32, B, "budget", dev),
+            self._stream(stream)))
+
+    def step_layer(self, layer, q, k_new, v_new, out, kept_pos=None, kept_count=None, stream=None):
+        """One layer of a begun step; buffers hold that layer only ([B, ...])."""
+        import torch
+        B, d, dev = self.B, self.d, self.device
+        args = [_dptr(q, torch.float16, B * self.Hq * d, "q", dev),
+                _dptr(k_new, torch.float16, B * self.Hkv * d, "k_new", dev),
+                _dptr(v_new, torch.float16, B * self.Hkv * d, "v_new", dev),
+                _dptr(out, torch.float32, B * self.Hq * d, "out", dev),
+                _dptr(kept_pos, torch.int32, B * self.Ncap, "kept_pos", dev),
+                _dptr(kept_count, torch.int32, B, "kept_count", dev)]
+        self._check(self._L.confkv_step_layer(self._h, layer, *args, self._stream(stream)))
 
     def step_host(self, logits, q, k_new, v_new, out, kept_pos=None, kept_count=None,
                   conf=None, budget=None, stream=None):

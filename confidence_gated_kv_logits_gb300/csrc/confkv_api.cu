@@ -44,7 +44,11 @@ struct DeviceGuard {
 struct confkv_ctx {
   int L = 0, B = 0, Hq = 0, Hkv = 0, d = 0, g = 0, V = 0;
   int N_low = 0, N_high = 0, P = 0, W = 0, Wr = 0, Ncap = 0, cap8 = 0, slots = 0;
-  int max_context = 0, device = 0, splits = 1, attn_kernel = 0;
+  int max_context = 0, device = 0, splits = 1, splits_layer = 1, attn_kernel = 0;
+  // per-layer stepping (confkv_step_begin / confkv_step_layer)
+  bool step_open = false;
+  int layers_left = 0;
+  std::vector<unsigned char> layer_done;
   float tau = 0.f, beta = 0.f, omb = 0.f, pyramid_min = 1.f;
   int64_t t = 0, steps = 0;
   bool prefilled = false;
@@ -138,13 +142,22 @@ void prof_collect(confkv_ctx* c) {
   }
 }
 
-int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s) {
+int auto_splits(int units, int ncap) {
+  const int want = (4 * kSmCount + units - 1) / units;
+  const int tok_lim = std::max(1, (ncap + 1 + 127) / 128);
+  return std::max(1, std::min(std::min(want, tok_lim), 16));
+}
+
+int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s, int lb0, int nlb,
+                  int splits) {
   AttnParams ap{};
+  ap.lb0 = lb0;
+  ap.nlb = nlb;
   ap.q = q;
   ap.out = out;
   ap.kernel = c->attn_kernel;
   ap.tmaps = c->has_tmaps ? c->tmaps : nullptr;
-  ap.splits = c->splits;
+  ap.splits = splits;
   ap.part_ml = c->part_ml;
   ap.part_acc = c->part_acc;
   ap.ticket = c->ticket;
@@ -207,12 +220,12 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   const size_t U = LB * c->Hkv;
   const int units = static_cast<int>(U);
   if (o.attn_splits > 0) {
-    c->splits = o.attn_splits;
+    c->splits = c->splits_layer = o.attn_splits;
   } else {
-    const int want = (4 * kSmCount + units - 1) / units;
-    const int tok_lim = std::max(1, (c->Ncap + 1 + 127) / 128);
-    c->splits = std::max(1, std::min(std::min(want, tok_lim), 16));
+    c->splits = auto_splits(units, c->Ncap);
+    c->splits_layer = auto_splits(c->B * c->Hkv, c->Ncap);
   }
+  const int max_splits = std::max(c->splits, c->splits_layer);
 
   Cache& k = c->cache;
   k.L = c->L; k.B = c->B; k.Hq = c->Hq; k.Hkv = c->Hkv; k.d = c->d; k.g = c->g;
@@ -241,8 +254,8 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   A(dalloc(c, &c->conf_part, static_cast<size_t>(c->B) * confkv::confidence_ctas_per_seq(c->B, c->V)));
   A(dalloc(c, &c->conf_ticket, c->B));
   A(dalloc(c, &c->btab, static_cast<size_t>(c->L) * 2));
-  A(dalloc(c, &c->part_ml, LB * c->Hq * c->splits * 2));
-  A(dalloc(c, &c->part_acc, LB * c->Hq * c->splits * c->d));
+  A(dalloc(c, &c->part_ml, LB * c->Hq * max_splits * 2));
+  A(dalloc(c, &c->part_acc, LB * c->Hq * max_splits * c->d));
   A(dalloc(c, &c->ticket, U));
 
   A(dalloc(c, &c->seed_out, LB * c->Hq * c->d));
@@ -263,6 +276,7 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
     delete c;
     return oom ? CONFKV_ERR_OOM : CONFKV_ERR_CUDA;
   }
+  c->layer_done.assign(c->L, 0);
   *out = c;
   return CONFKV_OK;
 }
@@ -270,7 +284,8 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
 int confkv_prefill(confkv_ctx* c, const uint16_t* k, const uint16_t* v, int T,
                    const uint16_t* q_last, void* stream) {
   if (!c) return CONFKV_ERR_INVALID_ARG;
-  if (c->steps > 0 || c->prefilled) return fail(c, CONFKV_ERR_STATE, "prefill must precede every step and happen once");
+  if (c->steps > 0 || c->prefilled || c->step_open)
+    return fail(c, CONFKV_ERR_STATE, "prefill must precede every step and happen once");
   if (T < 0) return fail(c, CONFKV_ERR_INVALID_ARG, "T < 0");
   if (T > c->max_context) return fail(c, CONFKV_ERR_CAPACITY, "T exceeds max_context");
   if (T > 0 && (!k || !v)) return fail(c, CONFKV_ERR_INVALID_ARG, "null k or v");
@@ -284,32 +299,48 @@ int confkv_prefill(confkv_ctx* c, const uint16_t* k, const uint16_t* v, int T,
   cudaError_t e = confkv::launch_prefill_store(c->cache, reinterpret_cast<const __half*>(k),
                                                reinterpret_cast<const __half*>(v), T, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("prefill: ") + cudaGetErrorString(e));
-  if (q_last) return run_attention(c, reinterpret_cast<const __half*>(q_last), c->seed_out, s);
+  if (q_last)
+    return run_attention(c, reinterpret_cast<const __half*>(q_last), c->seed_out, s, 0,
+                         c->L * c->B, c->splits);
   return CONFKV_OK;
 }
 
-int confkv_step(confkv_ctx* c, const float* logits, const uint16_t* q, const uint16_t* k_new,
-                const uint16_t* v_new, float* out, int32_t* kept_pos, int32_t* kept_count,
-                float* conf_out, int32_t* budget_out, void* stream) {
-  if (!c) return CONFKV_ERR_INVALID_ARG;
-  if (!logits || !q || !k_new || !v_new || !out)
-    return fail(c, CONFKV_ERR_INVALID_ARG, "null logits, q, k_new, v_new or out");
-  if (c->t >= 0x7fffffffLL) return fail(c, CONFKV_ERR_STATE, "position overflow");
+}  // extern "C"
+
+namespace {
+
+int check_layer_args(confkv_ctx* c, const uint16_t* q, const uint16_t* k_new,
+                     const uint16_t* v_new, float* out) {
+  if (!q || !k_new || !v_new || !out)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "null q, k_new, v_new or out");
   if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
     return fail(c, CONFKV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(out) |
-       reinterpret_cast<uintptr_t>(q)) & 3u)
-    return fail(c, CONFKV_ERR_INVALID_ARG, "misaligned logits, q or out");
-  DeviceGuard guard(c->device);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
+  if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(q)) & 3u)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "misaligned q or out");
+  return CONFKV_OK;
+}
+
+int run_confidence(confkv_ctx* c, const float* logits, float* conf_out, int32_t* budget_out,
+                   cudaStream_t s) {
+  if (reinterpret_cast<uintptr_t>(logits) & 3u)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "misaligned logits");
+  if (c->t >= 0x7fffffffLL) return fail(c, CONFKV_ERR_STATE, "position overflow");
   prof_mark(c, 0, s);
-  e = confkv::launch_confidence(logits, c->B, c->V, c->tau, c->N_low, c->N_high, c->conf, c->hi,
-                                conf_out, budget_out, c->cache.err, c->cache.stats,
-                                c->conf_part, c->conf_ticket, s);
+  const cudaError_t e = confkv::launch_confidence(
+      logits, c->B, c->V, c->tau, c->N_low, c->N_high, c->conf, c->hi, conf_out, budget_out,
+      c->cache.err, c->cache.stats, c->conf_part, c->conf_ticket, s);
   prof_mark(c, 0, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("confidence: ") + cudaGetErrorString(e));
+  return CONFKV_OK;
+}
+
+// selection + compaction + attention of the (layer, sequence) range [lb0, lb0 + nlb)
+int run_layers(confkv_ctx* c, int lb0, int nlb, int splits, const uint16_t* q,
+               const uint16_t* k_new, const uint16_t* v_new, float* out, int32_t* kept_pos,
+               int32_t* kept_count, cudaStream_t s) {
   StepParams sp{};
+  sp.lb0 = lb0;
+  sp.nlb = nlb;
   sp.t = static_cast<int>(c->t);
   sp.beta = c->beta;
   sp.omb = c->omb;
@@ -320,15 +351,71 @@ int confkv_step(confkv_ctx* c, const float* logits, const uint16_t* q, const uin
   sp.k_new = reinterpret_cast<const __half*>(k_new);
   sp.v_new = reinterpret_cast<const __half*>(v_new);
   prof_mark(c, 1, s);
-  e = confkv::launch_select(c->cache, sp, s);
+  const cudaError_t e = confkv::launch_select(c->cache, sp, s);
   prof_mark(c, 1, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("select: ") + cudaGetErrorString(e));
   prof_mark(c, 3, s);
-  const int rc = run_attention(c, reinterpret_cast<const __half*>(q), out, s);
+  const int rc = run_attention(c, reinterpret_cast<const __half*>(q), out, s, lb0, nlb, splits);
   prof_mark(c, 3, s);
+  return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int confkv_step(confkv_ctx* c, const float* logits, const uint16_t* q, const uint16_t* k_new,
+                const uint16_t* v_new, float* out, int32_t* kept_pos, int32_t* kept_count,
+                float* conf_out, int32_t* budget_out, void* stream) {
+  if (!c) return CONFKV_ERR_INVALID_ARG;
+  if (!logits) return fail(c, CONFKV_ERR_INVALID_ARG, "null logits");
+  int rc = check_layer_args(c, q, k_new, v_new, out);
+  if (rc != CONFKV_OK) return rc;
+  if (c->step_open) return fail(c, CONFKV_ERR_STATE, "a per-layer step is open");
+  DeviceGuard guard(c->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = run_confidence(c, logits, conf_out, budget_out, s);
+  if (rc != CONFKV_OK) return rc;
+  rc = run_layers(c, 0, c->L * c->B, c->splits, q, k_new, v_new, out, kept_pos, kept_count, s);
   if (rc != CONFKV_OK) return rc;
   c->t += 1;
   c->steps += 1;
+  return CONFKV_OK;
+}
+
+int confkv_step_begin(confkv_ctx* c, const float* logits, float* conf_out, int32_t* budget_out,
+                      void* stream) {
+  if (!c) return CONFKV_ERR_INVALID_ARG;
+  if (!logits) return fail(c, CONFKV_ERR_INVALID_ARG, "null logits");
+  if (c->step_open) return fail(c, CONFKV_ERR_STATE, "the previous step still has layers to run");
+  DeviceGuard guard(c->device);
+  const int rc = run_confidence(c, logits, conf_out, budget_out, static_cast<cudaStream_t>(stream));
+  if (rc != CONFKV_OK) return rc;
+  c->step_open = true;
+  c->layers_left = c->L;
+  std::fill(c->layer_done.begin(), c->layer_done.end(), 0);
+  return CONFKV_OK;
+}
+
+int confkv_step_layer(confkv_ctx* c, int layer, const uint16_t* q, const uint16_t* k_new,
+                      const uint16_t* v_new, float* out, int32_t* kept_pos, int32_t* kept_count,
+                      void* stream) {
+  if (!c) return CONFKV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= c->L) return fail(c, CONFKV_ERR_INVALID_ARG, "layer out of range");
+  int rc = check_layer_args(c, q, k_new, v_new, out);
+  if (rc != CONFKV_OK) return rc;
+  if (!c->step_open) return fail(c, CONFKV_ERR_STATE, "no step begun (confkv_step_begin)");
+  if (c->layer_done[layer]) return fail(c, CONFKV_ERR_STATE, "layer already run in this step");
+  DeviceGuard guard(c->device);
+  rc = run_layers(c, layer * c->B, c->B, c->splits_layer, q, k_new, v_new, out, kept_pos,
+                  kept_count, static_cast<cudaStream_t>(stream));
+  if (rc != CONFKV_OK) return rc;
+  c->layer_done[layer] = 1;
+  if (--c->layers_left == 0) {
+    c->step_open = false;
+    c->t += 1;
+    c->steps += 1;
+  }
   return CONFKV_OK;
 }
 

@@ -87,6 +87,8 @@ struct Cache {
 };
 
 struct StepParams {
+  int lb0, nlb;          // (layer, sequence) range of this launch: [lb0, lb0 + nlb);
+                         // the caller's buffers below start at lb0
   int t;                 // position of the new token
   float beta, omb;       // EMA decay and 1 - decay (fp32)
   const int32_t* btab;   // [L][2] per-layer budget for (N_low, N_high)
@@ -98,6 +100,7 @@ struct StepParams {
 };
 
 struct AttnParams {
+  int lb0, nlb;          // (layer, sequence) range; q and out start at lb0
   int kernel;             // 0 auto, 1 CUDA-core, 2 tensor-core
   const void* tmaps;     // host pointer to 4 CUtensorMap (K8, V8, K16, V16) or null
   const __half* q;       // [L*B][Hq][d]

@@ -44,8 +44,9 @@ __device__ __forceinline__ float rescale(float m_old, float m_new) {
 template <int D>
 __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap) {
   constexpr int DPL = D / 32;
-  const int unit = blockIdx.x, split = blockIdx.y;
+  const int unit = ap.lb0 * c.Hkv + blockIdx.x, split = blockIdx.y;
   const int lb = unit / c.Hkv, kvh = unit - lb * c.Hkv, g = c.g;
+  const int lbu = lb - ap.lb0;                // index into the caller's q / out
   const int n8 = c.n8[lb], n16 = c.n16[lb], n = n8 + n16;
   const int ntiles = (n + kTile - 1) / kTile;
   const int tps = (ntiles + ap.splits - 1) / ap.splits;
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
   float* fin = wl + kWarps * g;             // [2][g] final max, sum
   float* wacc = fin + 2 * g;                // [kWarps][g][D]
 
-  const size_t qbase = (static_cast<size_t>(lb) * c.Hq + kvh * g) * D;
+  const size_t qbase = (static_cast<size_t>(lbu) * c.Hq + kvh * g) * D;
   for (int i = tid; i < g * D; i += kThreads) qs[i] = __half2float(ap.q[qbase + i]);
   __syncthreads();
 
@@ -184,7 +185,8 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
     }
   }
   __syncthreads();
-  const size_t obase = (static_cast<size_t>(lb) * c.Hq + kvh * g);
+  const size_t obase = (static_cast<size_t>(lb) * c.Hq + kvh * g);   // split-K scratch
+  float* outp = ap.out + (static_cast<size_t>(lbu) * c.Hq + kvh * g) * D;
   for (int idx = tid; idx < g * D; idx += kThreads) {
     const int h = idx / D, dd = idx - h * D;
     float M = -INFINITY;
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
       A += wacc[(w * g + h) * D + dd] * f;
     }
     if (ap.splits == 1) {
-      ap.out[(obase + h) * D + dd] = A / Ls;
+      outp[h * D + dd] = A / Ls;
       if (dd == 0) { fin[h] = M; fin[g + h] = Ls; }
     } else {
       const size_t pi = (obase + h) * ap.splits + split;
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
         Ls += __ldcg(&ap.part_ml[(pb + sp) * 2 + 1]) * f;
         A += __ldcg(&ap.part_acc[(pb + sp) * D + dd]) * f;
       }
-      ap.out[(obase + h) * D + dd] = A / Ls;
+      outp[h * D + dd] = A / Ls;
       if (dd == 0) { fin[h] = M; fin[g + h] = Ls; }
     }
     if (tid == 0) ap.ticket[unit] = 0u;
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
 template <int D>
 cudaError_t launch_simple(const Cache& c, const AttnParams& ap, cudaStream_t s) {
   const size_t smem = sizeof(float) * (c.g * D + 2 * kWarps * c.g + 2 * c.g + kWarps * c.g * D);
-  k_attn_simple<D><<<dim3(c.L * c.B * c.Hkv, ap.splits), kThreads, smem, s>>>(c, ap);
+  k_attn_simple<D><<<dim3(ap.nlb * c.Hkv, ap.splits), kThreads, smem, s>>>(c, ap);
   return cudaGetLastError();
 }
 

@@ -287,14 +287,15 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   // 1024-byte aligned base (128-byte swizzle atoms)
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
-  const int unit = blockIdx.x, split = blockIdx.y;
+  const int unit = ap.lb0 * c.Hkv + blockIdx.x, split = blockIdx.y;
   const int lb = unit / c.Hkv, kvh = unit - lb * c.Hkv, g = c.g;
+  const int lbu = lb - ap.lb0;                // index into the caller's q / out
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, t4 = lane & 3;
   // Q^T operand: query gid, channels t4*KPT + 4kk + {0,1} and {2,3}
   uint32_t qb[G::KS][2];
   if (gid < g) {
     const uint4* qp = reinterpret_cast<const uint4*>(
-        ap.q + (static_cast<size_t>(lb) * c.Hq + kvh * g + gid) * D + t4 * G::KPT);
+        ap.q + (static_cast<size_t>(lbu) * c.Hq + kvh * g + gid) * D + t4 * G::KPT);
 #pragma unroll
     for (int j = 0; j < G::KS / 2; ++j) {
       const uint4 v = qp[j];
@@ -633,7 +634,8 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     ob[d0 + 1] = O[mt][3] * unscale;
   }
   __syncthreads();
-  const size_t obase = static_cast<size_t>(lb) * c.Hq + kvh * g;
+  const size_t obase = static_cast<size_t>(lb) * c.Hq + kvh * g;     // split-K scratch
+  float* outp = ap.out + (static_cast<size_t>(lbu) * c.Hq + kvh * g) * D;
   for (int idx = tid; idx < g * D; idx += kThreads) {
     const int h = idx / D, dd = idx - h * D;
     float M = -INFINITY;
@@ -645,7 +647,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       A += wo[(w * 8 + h) * D + dd] * f;
     }
     if (ap.splits == 1) {
-      ap.out[(obase + h) * D + dd] = A / Ls;
+      outp[h * D + dd] = A / Ls;
       if (dd == 0) { fin[h] = M; fin[8 + h] = Ls; }
     } else {
       const size_t pi = (obase + h) * ap.splits + split;
@@ -672,7 +674,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
         Ls += __ldcg(&ap.part_ml[(pb + sp) * 2 + 1]) * f;
         A += __ldcg(&ap.part_acc[(pb + sp) * D + dd]) * f;
       }
-      ap.out[(obase + h) * D + dd] = A / Ls;
+      outp[h * D + dd] = A / Ls;
       if (dd == 0) { fin[h] = M; fin[8 + h] = Ls; }
     }
     if (tid == 0) ap.ticket[unit] = 0u;
@@ -722,7 +724,7 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const cudaError_t e = launch_pdl(k_attn_mma<D, TMA>, dim3(c.L * c.B * c.Hkv, ap.splits),
+  const cudaError_t e = launch_pdl(k_attn_mma<D, TMA>, dim3(ap.nlb * c.Hkv, ap.splits),
                                    dim3(kThreads), smem, s, c, ap, tm);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

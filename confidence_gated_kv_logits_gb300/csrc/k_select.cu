@@ -139,7 +139,8 @@ __device__ void quantize_row_warp(const __half* src, int8_t* dst, float* scale_o
 }
 
 __global__ void __launch_bounds__(kThreads, 4) k_select(Cache c, StepParams sp) {
-  const int lb = blockIdx.x;
+  const int lb = sp.lb0 + blockIdx.x;
+  const int lbu = blockIdx.x;                 // index into the caller's buffers
   const int l = lb / c.B, b = lb % c.B;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_trigger();     // the attention may be scheduled (it waits for this grid)
@@ -449,7 +450,8 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
           const int ch = isv ? pc - cpr : pc;
           __half* rows = (isv ? c.v16 : c.k16) + u8 * c.Wr * d;
           const __half* src = (jb.y >= 0) ? rows + static_cast<size_t>(jb.y) * d
-                                          : (isv ? sp.v_new : sp.k_new) + u8 * d;
+                                          : (isv ? sp.v_new : sp.k_new) +
+                                                (static_cast<size_t>(lbu) * Hkv + h) * d;
           v[u] = reinterpret_cast<const int4*>(src)[ch];
           dst[u] = rows + static_cast<size_t>(jb.x) * d + 8 * ch;
         }
@@ -473,7 +475,7 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
 
   // ---- outputs ----
   if (sp.kept_pos) {
-    int32_t* __restrict__ kp = sp.kept_pos + static_cast<size_t>(lb) * c.Ncap;
+    int32_t* __restrict__ kp = sp.kept_pos + static_cast<size_t>(lbu) * c.Ncap;
     for (int base = 0; base < n8n + n16n; base += 4 * kThreads) {
       int v[4];
 #pragma unroll
@@ -489,7 +491,7 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
     }
   }
   if (tid == 0) {
-    if (sp.kept_count) sp.kept_count[lb] = n8n + n16n;
+    if (sp.kept_count) sp.kept_count[lbu] = n8n + n16n;
     c.n8[lb] = n8n;
     c.n16[lb] = n16n;
     atomicAdd(&c.stats->evicted, static_cast<unsigned long long>(n_tot - n8n - n16n));
@@ -520,7 +522,7 @@ cudaError_t launch_select(const Cache& c, const StepParams& sp, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     attr = smem;
   }
-  const cudaError_t e = launch_pdl(k_select, dim3(c.L * c.B), dim3(kThreads), smem, s, c, sp);
+  const cudaError_t e = launch_pdl(k_select, dim3(sp.nlb), dim3(kThreads), smem, s, c, sp);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

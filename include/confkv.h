@@ -161,6 +161,32 @@ int confkv_step(confkv_ctx* ctx, const float* logits, const uint16_t* q,
                 int32_t* budget_out, void* stream);
 
 /*
+ * Per-layer stepping, for a model that produces one layer's q / k / v at a
+ * time (the layers of a decode step are not all known up front):
+ *
+ * confkv_step_begin -- first stage of a decode step: the confidence and the
+ * budget of every sequence from this step's logits (as in confkv_step).
+ *   logits fp32 [B][V]; conf_out fp32 [B] and budget_out int32 [B] may be NULL.
+ * CONFKV_ERR_STATE if the previous begun step still has layers to run.
+ *
+ * confkv_step_layer -- the rest of the step for one layer `layer`: EMA update,
+ * ranking, eviction, compaction + INT8 aging and attention of that layer's B
+ * caches.  Buffers hold that layer only:
+ *   q fp16 [B][Hq][d]; k_new, v_new fp16 [B][Hkv][d] (16-byte aligned);
+ *   out fp32 [B][Hq][d]; kept_pos int32 [B][N_max] and kept_count int32 [B]
+ *   may be NULL.
+ * Every layer must be run exactly once, in any order; the step (and the
+ * position) advances after the last one.  CONFKV_ERR_STATE without a begun
+ * step or for a layer already run; CONFKV_ERR_INVALID_ARG for a bad layer.
+ * The results equal confkv_step's for the same inputs.
+ */
+int confkv_step_begin(confkv_ctx* ctx, const float* logits, float* conf_out,
+                      int32_t* budget_out, void* stream);
+int confkv_step_layer(confkv_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
+                      const uint16_t* v_new, float* out, int32_t* kept_pos,
+                      int32_t* kept_count, void* stream);
+
+/*
  * confkv_step_host -- confkv_step with HOST buffers of the same layouts.
  * Copies the inputs to context-owned device staging buffers, runs the step
  * and copies the outputs back, all on `stream`, then waits for the stream.

@@ -76,7 +76,7 @@ def compare_cache(kv, orc, l, b, rep):
 
 
 def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, splits=0,
-        logits_override=None, kernel=0, tma=0):
+        logits_override=None, kernel=0, tma=0, per_layer=False):
     """Run workload `w` on the GPU and in the oracle; return a Report.
 
     lbs: iterable of (l, b) the oracle simulates (default: all).
@@ -134,7 +134,17 @@ def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, spli
             glg, gq, gk, gv = sd.step_inputs(w, s)
         else:
             glg, gq, gk, gv = (to_dev(x, dev) for x in (lg, q, k, v))
-        kv.step(glg, gq, gk, gv, out, kp, kc, cf, bd)
+        if per_layer:        # confkv_step_begin + one confkv_step_layer per layer, reversed
+            kv.step_begin(glg, cf, bd)
+            for l in reversed(range(w.L)):
+                ol = torch.empty(w.B, w.Hq, w.d, device=dev)
+                kpl = torch.full((w.B, kv.Ncap), -1, dtype=torch.int32, device=dev)
+                kcl = torch.zeros(w.B, dtype=torch.int32, device=dev)
+                kv.step_layer(l, gq[l].contiguous(), gk[l].contiguous(), gv[l].contiguous(), ol,
+                              kpl, kcl)
+                out[l], kp[l], kc[l] = ol, kpl, kcl
+        else:
+            kv.step(glg, gq, gk, gv, out, kp, kc, cf, bd)
         r = orc.step(lg, q, k, v, cap=kv.Ncap)
         torch.cuda.synchronize()
         g_out, g_kp, g_kc = out.cpu().numpy(), kp.cpu().numpy(), kc.cpu().numpy()
