@@ -28,6 +28,14 @@ namespace confkv {
 // wait returns once that grid has completed and its memory is visible), and
 // pdl_trigger() once its own dependents may be scheduled.  Without the launch
 // attribute both are no-ops.
+// Drops one 128-byte line from L2 without writing it back: for scratch that
+// has been read for the last time before its next full rewrite (PTX
+// `discard.global.L2`; the line's contents become undefined).  `p` must be
+// 128-byte aligned and the line must hold nothing else that is still live.
+__device__ __forceinline__ void l2_discard_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;\n" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");

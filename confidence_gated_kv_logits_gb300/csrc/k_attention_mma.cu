@@ -708,6 +708,19 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
           a.z += ex2(fmaf(sv[h].z, kL2E, -ML[h])) * iL[h];
           a.w += ex2(fmaf(sv[h].w, kL2E, -ML[h])) * iL[h];
         }
+      // The raw scores are dead once read here (the next step rewrites every
+      // live slot before reading it): drop whole 128-byte lines of them from
+      // L2 so they are never written back.  The 8 lanes reading one line are
+      // in this warp; lines shared with a neighbouring row are kept.
+      __syncwarp(__activemask());
+      if ((j & 7) == 0 && 4 * j + 32 <= cnt_r) {
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+          if (h < g) {
+            const float* line = SC + static_cast<size_t>(h) * c.slots + base + 4 * j;
+            if ((reinterpret_cast<uintptr_t>(line) & 127u) == 0) l2_discard_line(line);
+          }
+      }
       // slots past the region end hold stale scores; their mass is never read
       reinterpret_cast<float4*>(MS + base)[j] = a;
     }

@@ -234,6 +234,17 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
   pdl_wait();        // the confidence kernel's budget flags are complete
   const int N = sp.btab[l * 2 + (sp.hi[b] ? 1 : 0)];
   __syncthreads();
+  // Every thread has read the previous attention's per-token mass, which this
+  // step's attention rewrites for every live slot before the next read: drop
+  // its whole 128-byte lines from L2 without a write-back.
+  {
+    const int l8 = n8 >> 5, l16 = n16 >> 5, per = l8 + l16;
+    for (int x = tid; x < Hkv * per; x += kThreads) {
+      const int h = x / per, r = x - h * per;
+      const float* line = mass + static_cast<size_t>(h) * c.slots + (r < l8 ? 32 * r : cap8 + 32 * (r - l8));
+      if ((reinterpret_cast<uintptr_t>(line) & 127u) == 0) l2_discard_line(line);
+    }
+  }
   const int pcount = s_prot + 1;            // + the new token
   const int jage = s_jage;
   const int n_tot = ntok + 1;
