@@ -75,7 +75,7 @@ struct confkv_ctx {
   float* st_conf = nullptr;
   int32_t* st_bud = nullptr;
   std::string msg = "ok";
-  alignas(64) unsigned char tmaps[512];          // tensor maps of the d = 128 TMA path
+  alignas(64) unsigned char tmaps[confkv::kTmaMapsBytes];          // tensor maps of the d = 128 TMA path
   bool has_tmaps = false;
   // profiling
   int prof = 0;                                 // kernel bit mask
@@ -315,8 +315,10 @@ int check_layer_args(confkv_ctx* c, const uint16_t* q, const uint16_t* k_new,
     return fail(c, CONFKV_ERR_INVALID_ARG, "null q, k_new, v_new or out");
   if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
     return fail(c, CONFKV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(q)) & 3u)
-    return fail(c, CONFKV_ERR_INVALID_ARG, "misaligned q or out");
+  if (reinterpret_cast<uintptr_t>(q) & 15u)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(out) & 3u)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "misaligned out");
   return CONFKV_OK;
 }
 

@@ -132,7 +132,9 @@ cudaError_t launch_prefill_store(const Cache& c, const __half* k, const __half* 
 cudaError_t launch_attention(const Cache& c, const AttnParams& ap, cudaStream_t s);
 cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStream_t s);
 // Encodes the four tensor maps of the d = 128 TMA attention path into `out`
-// (4 CUtensorMap, 512 bytes); returns false if the driver cannot.
+// (kTmaMapsBytes bytes, 64-byte aligned); returns false if the driver cannot
+// or the cache is too large for 32-bit tile coordinates.
+constexpr int kTmaMapsBytes = 512;
 bool encode_attention_maps(const Cache& c, void* out);
 
 }  // namespace confkv

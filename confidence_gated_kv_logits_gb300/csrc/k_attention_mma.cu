@@ -746,6 +746,11 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
 
 bool encode_attention_maps(const Cache& c, void* out) {
   if (c.d != 128) return false;
+  {
+    // tile coordinates are signed 32-bit
+    const unsigned long long u = static_cast<unsigned long long>(c.L) * c.B * c.Hkv;
+    if (u * c.cap8 >= (1ull << 31) || u * c.Wr >= (1ull << 31)) return false;
+  }
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
@@ -787,6 +792,7 @@ bool encode_attention_maps(const Cache& c, void* out) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
   }
+  static_assert(sizeof(TmaMaps) <= kTmaMapsBytes, "tensor-map blob size");
   std::memcpy(out, &tm, sizeof(tm));
   return true;
 }

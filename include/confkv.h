@@ -141,8 +141,9 @@ int confkv_prefill(confkv_ctx* ctx, const uint16_t* k, const uint16_t* v, int T,
  * confkv_step -- one decode step of every (layer, sequence): confidence,
  * budget, EMA + ranking, eviction, compaction + INT8 aging, attention.
  *   logits:  fp32 [B][V]          this step's next-token logits
- *   q:       fp16 [L][B][Hq][d]   queries of the new token
- *   k_new:   fp16 [L][B][Hkv][d]  key of the new token (appended, FP16)
+ *   q:       fp16 [L][B][Hq][d]   queries of the new token (16-byte aligned)
+ *   k_new:   fp16 [L][B][Hkv][d]  key of the new token (appended, FP16;
+ *                                 16-byte aligned, as is v_new)
  *   v_new:   fp16 [L][B][Hkv][d]
  *   out:     fp32 [L][B][Hq][d]   attention output over the kept cache
  *   kept_pos:   int32 [L][B][N_max], N_max = max(N_low, N_high): positions of
@@ -172,7 +173,7 @@ int confkv_step(confkv_ctx* ctx, const float* logits, const uint16_t* q,
  * confkv_step_layer -- the rest of the step for one layer `layer`: EMA update,
  * ranking, eviction, compaction + INT8 aging and attention of that layer's B
  * caches.  Buffers hold that layer only:
- *   q fp16 [B][Hq][d]; k_new, v_new fp16 [B][Hkv][d] (16-byte aligned);
+ *   q fp16 [B][Hq][d]; k_new, v_new fp16 [B][Hkv][d] (all three 16-byte aligned);
  *   out fp32 [B][Hq][d]; kept_pos int32 [B][N_max] and kept_count int32 [B]
  *   may be NULL.
  * Every layer must be run exactly once, in any order; the step (and the

@@ -83,6 +83,11 @@ def test_per_layer_state_errors():
     with pytest.raises(pkg.ConfKVError) as e:
         kv.step_layer(w.L, q, k, k, o)                     # bad layer
     assert e.value.code == pkg.ERR_INVALID_ARG
+    qbuf = torch.zeros(q.numel() + 8, dtype=torch.float16, device=DEV)
+    q_mis = qbuf[4:4 + q.numel()].view(q.shape)            # 8-byte aligned only
+    with pytest.raises(pkg.ConfKVError) as e:
+        kv.step_layer(1, q_mis, k, k, o)                   # q must be 16-byte aligned
+    assert e.value.code == pkg.ERR_INVALID_ARG
     kv.step_layer(1, q, k, k, o)
     with pytest.raises(pkg.ConfKVError) as e:
         kv.step_layer(1, q, k, k, o)                       # layer twice
