@@ -115,6 +115,31 @@ __device__ int plan_warp(const unsigned* bits, int n, int extra, int2* jobs, int
   return mtot;
 }
 
+// The fp32 steps of the INT8 absmax quantiser of one fp16 row of d = 32 * per
+// elements, lane holding elements lane * per + j: amax over the row, scale =
+// amax / 127, code = round-half-even(x / scale) clamped to +-127, stored
+// offset-binary (code + 128).  Byte j of the result is element lane*per + j.
+__device__ __forceinline__ uint32_t quantize_lane(const float (&x)[4], int per, float& scale) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (j < per) amax = fmaxf(amax, fabsf(x[j]));
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = __fdiv_rn(amax, 127.0f);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int q = 0;
+    if (j < per && s != 0.0f) {
+      q = __float2int_rn(__fdiv_rn(x[j], s));
+      q = max(-127, min(127, q));
+    }
+    packed |= static_cast<uint32_t>((q ^ 0x80) & 0xff) << (8 * j);
+  }
+  scale = s;
+  return packed;
+}
+
 // warp-level INT8 absmax quantisation of one fp16 row of d elements
 __device__ void quantize_row_warp(const __half* src, int8_t* dst, float* scale_out, int d) {
   const int lane = threadIdx.x & 31;
@@ -247,6 +272,29 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
   }
   const int pcount = s_prot + 1;            // + the new token
   const int jage = s_jage;
+  // The token leaving the FP16 window (age W) is quantised now, before the
+  // selection decides whether it stays, so that its row loads and divisions
+  // overlap the selection; its codes are stored once its INT8 slot is known.
+  // Warp w takes rows w and w + kWarps of the 2 * Hkv (K, V) rows.
+  constexpr int kQRows = 2;
+  const bool early_q = jage >= 0 && 2 * Hkv <= kWarps * kQRows;
+  uint32_t qcode[kQRows] = {0u, 0u};
+  float qscale[kQRows] = {0.0f, 0.0f};
+  if (early_q) {
+    const int per = d / 32;                 // 2 or 4
+    float xr[kQRows][4];
+#pragma unroll
+    for (int rr = 0; rr < kQRows; ++rr) {
+      const int row = warp + rr * kWarps;
+      const int h = row >> 1;
+      const __half* src = ((row & 1) ? c.v16 : c.k16) +
+                          ((static_cast<size_t>(lb) * Hkv + h) * c.Wr + jage) * d + lane * per;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xr[rr][j] = (row < 2 * Hkv && j < per) ? __half2float(src[j]) : 0.0f;
+    }
+#pragma unroll
+    for (int rr = 0; rr < kQRows; ++rr) qcode[rr] = quantize_lane(xr[rr], per, qscale[rr]);
+  }
   const int n_tot = ntok + 1;
   // keep rule for candidates: mode 0 keep all, 1 keep none,
   // 2 (key & mask) >= prefix, 3 key != kmin (exactly one eviction)
@@ -295,15 +343,39 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
           }
         }
         __syncthreads();
-        if (tid == 0) {
-          int cum = 0, D = 0;
-          for (D = 255; D > 0; --D) {
-            if (cum + s_hist[D] >= k) break;
-            cum += s_hist[D];
+        if (warp == 0) {
+          // the highest bucket D whose count from the top reaches k: lane q
+          // holds buckets 255 - 8q .. 248 - 8q; scan across lanes, then within
+          // the first lane whose running total reaches k (one always does:
+          // the candidates under the prefix number at least k)
+          int h8[8], sum = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            h8[j] = s_hist[255 - 8 * lane - j];
+            sum += h8[j];
           }
-          s_D = D;
-          s_k = k - cum;
-          s_cnt = s_hist[D];
+          int incl = sum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
+          }
+          const unsigned reach = __ballot_sync(0xffffffffu, incl >= k);
+          const int first = reach ? __ffs(reach) - 1 : 31;
+          if (lane == first) {
+            int cum = incl - sum, D = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (cum + h8[j] >= k || 8 * lane + j == 255) {     // bucket 0 is the last resort
+                D = 255 - 8 * lane - j;
+                break;
+              }
+              cum += h8[j];
+            }
+            s_D = D;
+            s_k = k - cum;
+            s_cnt = s_hist[D];
+          }
         }
         __syncthreads();
         prefix |= static_cast<unsigned long long>(s_D) << shift;
@@ -428,15 +500,31 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
       pos8[hage] = pos16[jage];
       ema8[hage] = ema16[jage];
     }
-    // the aging token's K/V rows: quantise FP16 slot jage into INT8 slot hage
-    for (int row = warp; row < 2 * Hkv; row += kWarps) {
-      const int h = row >> 1;
-      const bool isv = row & 1;
-      const size_t u8 = static_cast<size_t>(lb) * Hkv + h;
-      const __half* src = (isv ? c.v16 : c.k16) + (u8 * c.Wr + jage) * d;
-      int8_t* dst = (isv ? c.v8 : c.k8) + (u8 * cap8 + hage) * d;
-      float* sc = (isv ? c.vs : c.ks) + u8 * cap8 + hage;
-      quantize_row_warp(src, dst, sc, d);
+    // the aging token's K/V rows: FP16 slot jage -> INT8 slot hage
+    if (early_q) {
+      const int per = d / 32;
+#pragma unroll
+      for (int rr = 0; rr < kQRows; ++rr) {
+        const int row = warp + rr * kWarps;
+        if (row < 2 * Hkv) {
+          const bool isv = row & 1;
+          const size_t u8 = static_cast<size_t>(lb) * Hkv + (row >> 1);
+          int8_t* dst = (isv ? c.v8 : c.k8) + (u8 * cap8 + hage) * d + lane * per;
+          if (per == 4) *reinterpret_cast<uint32_t*>(dst) = qcode[rr];
+          else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(qcode[rr]);
+          if (lane == 0) ((isv ? c.vs : c.ks) + u8 * cap8)[hage] = qscale[rr];
+        }
+      }
+    } else {
+      for (int row = warp; row < 2 * Hkv; row += kWarps) {
+        const int h = row >> 1;
+        const bool isv = row & 1;
+        const size_t u8 = static_cast<size_t>(lb) * Hkv + h;
+        const __half* src = (isv ? c.v16 : c.k16) + (u8 * c.Wr + jage) * d;
+        int8_t* dst = (isv ? c.v8 : c.k8) + (u8 * cap8 + hage) * d;
+        float* sc = (isv ? c.vs : c.ks) + u8 * cap8 + hage;
+        quantize_row_warp(src, dst, sc, d);
+      }
     }
   }
   __syncthreads();
