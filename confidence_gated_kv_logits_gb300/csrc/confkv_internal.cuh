@@ -22,12 +22,6 @@
 
 namespace confkv {
 
-// Programmatic dependent launch.  The step kernels are launched so that each
-// may start while its predecessor in the stream is still running: a kernel
-// calls pdl_wait() before it touches anything the predecessor writes (the
-// wait returns once that grid has completed and its memory is visible), and
-// pdl_trigger() once its own dependents may be scheduled.  Without the launch
-// attribute both are no-ops.
 // Drops one 128-byte line from L2 without writing it back: for scratch that
 // has been read for the last time before its next full rewrite (PTX
 // `discard.global.L2`; the line's contents become undefined).  `p` must be
@@ -36,6 +30,17 @@ __device__ __forceinline__ void l2_discard_line(const void* p) {
   asm volatile("discard.global.L2 [%0], 128;\n" ::"l"(p) : "memory");
 }
 
+// Programmatic dependent launch.  The step kernels are launched so that each
+// may start while its predecessor in the stream is still running: a kernel
+// calls pdl_wait() before it touches anything the predecessor writes (the
+// wait returns once that grid has completed and its memory is visible), and
+// pdl_trigger() once its own dependents may be scheduled.  Without the launch
+// attribute both are no-ops.  Every kernel waits before it completes, so a
+// grid's completion implies that of every earlier kernel in the stream.  The
+// confidence kernel triggers right after its own wait and the attention after
+// its main loop; the selection kernel triggers at its start, which is safe
+// because the attention reads nothing but its caller's queries before its
+// wait.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
