@@ -24,6 +24,7 @@ ERR_CAPACITY = -4
 ERR_NONFINITE_LOGITS = -5
 ERR_STATE = -6
 ERR_DEVICE = -7
+POLICY_CONFKV, POLICY_WINDOW, POLICY_H2O, POLICY_RANDOM = 0, 1, 2, 3
 FLAG_NONFINITE = 1
 FLAG_CAPACITY = 2
 FLAG_TIMEOUT = 4
@@ -45,7 +46,8 @@ class Opts(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("vocab", ctypes.c_int),
                 ("max_context", ctypes.c_int), ("pyramid_min", ctypes.c_float),
                 ("device", ctypes.c_int), ("attn_splits", ctypes.c_int),
-                ("attn_kernel", ctypes.c_int), ("attn_tma", ctypes.c_int)]
+                ("attn_kernel", ctypes.c_int), ("attn_tma", ctypes.c_int),
+                ("policy", ctypes.c_int), ("reserved", ctypes.c_int), ("seed", ctypes.c_uint64)]
 
 
 class Stats(ctypes.Structure):
@@ -135,13 +137,14 @@ class ConfKV:
 
     def __init__(self, layers, heads, kv_heads, head_dim, N_low, N_high, tau, P, W,
                  ema_decay, *, batch=1, vocab, max_context=0, pyramid_min=1.0,
-                 device=None, attn_splits=0, attn_kernel=0, attn_tma=0):
+                 device=None, attn_splits=0, attn_kernel=0, attn_tma=0, policy=0, seed=0):
         import torch
         self._L = load_library()
         dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         self.device = dev
         opts = Opts(batch, vocab, max_context, pyramid_min, dev.index, attn_splits, attn_kernel,
-                    attn_tma)
+                    attn_tma, policy, 0, seed)
+        self.policy = policy
         h = ctypes.c_void_p()
         rc = self._L.confkv_create(layers, heads, kv_heads, head_dim, N_low, N_high, tau, P,
                                    W, ema_decay, ctypes.byref(opts), ctypes.byref(h))

@@ -50,6 +50,8 @@ struct confkv_ctx {
   int layers_left = 0;
   std::vector<unsigned char> layer_done;
   float tau = 0.f, beta = 0.f, omb = 0.f, pyramid_min = 1.f;
+  int policy = CONFKV_POLICY_CONFKV;
+  uint64_t seed = 0;
   int64_t t = 0, steps = 0;
   bool prefilled = false;
   Cache cache{};
@@ -142,6 +144,9 @@ void prof_collect(confkv_ctx* c) {
   }
 }
 
+// WINDOW keeps a fixed budget (N_low) and computes no confidence
+bool uses_confidence(const confkv_ctx* c) { return c->policy != CONFKV_POLICY_WINDOW; }
+
 int auto_splits(int units, int ncap) {
   const int want = (4 * kSmCount + units - 1) / units;
   const int tok_lim = std::max(1, (ncap + 1 + 127) / 128);
@@ -162,6 +167,9 @@ int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s, in
   ap.part_acc = c->part_acc;
   ap.ticket = c->ticket;
   ap.scale = 1.0f / std::sqrt(static_cast<float>(c->d));
+  // the per-token attention mass feeds only the EMA (CONF-KV) and the
+  // accumulated mass (H2O)
+  ap.mass = (c->policy == CONFKV_POLICY_CONFKV || c->policy == CONFKV_POLICY_H2O) ? 1 : 0;
   const cudaError_t e = confkv::launch_attention(c->cache, ap, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("attention launch: ") + cudaGetErrorString(e));
   return CONFKV_OK;
@@ -186,7 +194,8 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
       !std::isfinite(tau) || o.batch < 1 || o.vocab < 2 || o.max_context < 0 ||
       !(pmin > 0.0f && pmin <= 1.0f) || o.attn_splits < 0 || o.attn_splits > 64 ||
       o.attn_kernel < 0 || o.attn_kernel > 2 || o.attn_tma < -1 || o.attn_tma > 0 ||
-      (o.attn_kernel == 2 && heads / kv_heads > 8))
+      (o.attn_kernel == 2 && heads / kv_heads > 8) || o.policy < CONFKV_POLICY_CONFKV ||
+      o.policy > CONFKV_POLICY_RANDOM || o.reserved != 0)
     return CONFKV_ERR_INVALID_ARG;
   int dev = o.device;
   if (!opts || dev < 0) cudaGetDevice(&dev);
@@ -210,8 +219,13 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   c->max_context = o.max_context;
   c->device = dev;
   c->attn_kernel = o.attn_kernel;
+  c->policy = o.policy;
+  c->seed = o.seed;
   c->Ncap = std::max(N_low, N_high);
-  c->cap8 = std::max(std::max(0, o.max_context - W), c->Ncap);
+  // INT8 slots: the prefill's tokens older than W, and the kept tokens older
+  // than W (under WINDOW the kept tokens are the newest N_low)
+  const int kept_old = (o.policy == CONFKV_POLICY_WINDOW) ? std::max(0, N_low - W) : c->Ncap;
+  c->cap8 = std::max(std::max(0, o.max_context - W), std::max(kept_old, 32));
   c->cap8 = (c->cap8 + 31) / 32 * 32;
   c->Wr = (W + 15) / 16 * 16;
   c->slots = c->cap8 + c->Wr;
@@ -352,6 +366,8 @@ int run_layers(confkv_ctx* c, int lb0, int nlb, int splits, const uint16_t* q,
   sp.kept_count = kept_count;
   sp.k_new = reinterpret_cast<const __half*>(k_new);
   sp.v_new = reinterpret_cast<const __half*>(v_new);
+  sp.policy = c->policy;
+  sp.seed = c->seed;
   prof_mark(c, 1, s);
   const cudaError_t e = confkv::launch_select(c->cache, sp, s);
   prof_mark(c, 1, s);
@@ -370,14 +386,16 @@ int confkv_step(confkv_ctx* c, const float* logits, const uint16_t* q, const uin
                 const uint16_t* v_new, float* out, int32_t* kept_pos, int32_t* kept_count,
                 float* conf_out, int32_t* budget_out, void* stream) {
   if (!c) return CONFKV_ERR_INVALID_ARG;
-  if (!logits) return fail(c, CONFKV_ERR_INVALID_ARG, "null logits");
+  if (!logits && uses_confidence(c)) return fail(c, CONFKV_ERR_INVALID_ARG, "null logits");
   int rc = check_layer_args(c, q, k_new, v_new, out);
   if (rc != CONFKV_OK) return rc;
   if (c->step_open) return fail(c, CONFKV_ERR_STATE, "a per-layer step is open");
   DeviceGuard guard(c->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = run_confidence(c, logits, conf_out, budget_out, s);
-  if (rc != CONFKV_OK) return rc;
+  if (uses_confidence(c)) {
+    rc = run_confidence(c, logits, conf_out, budget_out, s);
+    if (rc != CONFKV_OK) return rc;
+  }
   rc = run_layers(c, 0, c->L * c->B, c->splits, q, k_new, v_new, out, kept_pos, kept_count, s);
   if (rc != CONFKV_OK) return rc;
   c->t += 1;
@@ -388,11 +406,13 @@ int confkv_step(confkv_ctx* c, const float* logits, const uint16_t* q, const uin
 int confkv_step_begin(confkv_ctx* c, const float* logits, float* conf_out, int32_t* budget_out,
                       void* stream) {
   if (!c) return CONFKV_ERR_INVALID_ARG;
-  if (!logits) return fail(c, CONFKV_ERR_INVALID_ARG, "null logits");
+  if (!logits && uses_confidence(c)) return fail(c, CONFKV_ERR_INVALID_ARG, "null logits");
   if (c->step_open) return fail(c, CONFKV_ERR_STATE, "the previous step still has layers to run");
   DeviceGuard guard(c->device);
-  const int rc = run_confidence(c, logits, conf_out, budget_out, static_cast<cudaStream_t>(stream));
-  if (rc != CONFKV_OK) return rc;
+  if (uses_confidence(c)) {
+    const int rc = run_confidence(c, logits, conf_out, budget_out, static_cast<cudaStream_t>(stream));
+    if (rc != CONFKV_OK) return rc;
+  }
   c->step_open = true;
   c->layers_left = c->L;
   std::fill(c->layer_done.begin(), c->layer_done.end(), 0);
@@ -426,7 +446,7 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
                      int32_t* kept_pos, int32_t* kept_count, float* conf_out,
                      int32_t* budget_out, void* stream) {
   if (!c) return CONFKV_ERR_INVALID_ARG;
-  if (!logits || !q || !k_new || !v_new || !out)
+  if ((!logits && uses_confidence(c)) || !q || !k_new || !v_new || !out)
     return fail(c, CONFKV_ERR_INVALID_ARG, "null logits, q, k_new, v_new or out");
   DeviceGuard guard(c->device);
   const size_t LB = static_cast<size_t>(c->L) * c->B;
@@ -447,12 +467,12 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     if (e != cudaSuccess) return fail(c, e == cudaErrorMemoryAllocation ? CONFKV_ERR_OOM : CONFKV_ERR_CUDA, "staging allocation");
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  A(cudaMemcpyAsync(c->st_logits, logits, nlog * sizeof(float), cudaMemcpyHostToDevice, s));
+  if (logits) A(cudaMemcpyAsync(c->st_logits, logits, nlog * sizeof(float), cudaMemcpyHostToDevice, s));
   A(cudaMemcpyAsync(c->st_q, q, nq * 2, cudaMemcpyHostToDevice, s));
   A(cudaMemcpyAsync(c->st_k, k_new, nkv * 2, cudaMemcpyHostToDevice, s));
   A(cudaMemcpyAsync(c->st_v, v_new, nkv * 2, cudaMemcpyHostToDevice, s));
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("H2D: ") + cudaGetErrorString(e));
-  const int rc = confkv_step(c, c->st_logits, c->st_q, c->st_k, c->st_v, c->st_out,
+  const int rc = confkv_step(c, logits ? c->st_logits : nullptr, c->st_q, c->st_k, c->st_v, c->st_out,
                              kept_pos ? c->st_kp : nullptr, kept_count ? c->st_kc : nullptr,
                              conf_out ? c->st_conf : nullptr, budget_out ? c->st_bud : nullptr,
                              stream);
@@ -460,8 +480,10 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
   A(cudaMemcpyAsync(out, c->st_out, nq * sizeof(float), cudaMemcpyDeviceToHost, s));
   if (kept_pos) A(cudaMemcpyAsync(kept_pos, c->st_kp, nkp * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
   if (kept_count) A(cudaMemcpyAsync(kept_count, c->st_kc, LB * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
-  if (conf_out) A(cudaMemcpyAsync(conf_out, c->st_conf, c->B * sizeof(float), cudaMemcpyDeviceToHost, s));
-  if (budget_out) A(cudaMemcpyAsync(budget_out, c->st_bud, c->B * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  if (conf_out && uses_confidence(c))
+    A(cudaMemcpyAsync(conf_out, c->st_conf, c->B * sizeof(float), cudaMemcpyDeviceToHost, s));
+  if (budget_out && uses_confidence(c))
+    A(cudaMemcpyAsync(budget_out, c->st_bud, c->B * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
   A(cudaStreamSynchronize(s));
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("D2H: ") + cudaGetErrorString(e));
   return CONFKV_OK;

@@ -110,6 +110,8 @@ struct StepParams {
   int32_t* kept_count;   // [L*B] or null
   const __half* k_new;   // [L*B][Hkv][d] key / value of the new token
   const __half* v_new;
+  int policy;            // CONFKV_POLICY_*: ranking key and EMA rule
+  uint64_t seed;         // RANDOM policy draws
 };
 
 struct AttnParams {
@@ -123,6 +125,7 @@ struct AttnParams {
   float* part_acc;       // [L*B*Hq][splits][d]
   unsigned int* ticket;  // [L*B*Hkv]
   float scale;           // 1/sqrt(d)
+  int mass;              // 1: write the per-token attention mass (EMA / H2O policies)
 };
 
 // ---- launch wrappers (each file owns its kernels) ----

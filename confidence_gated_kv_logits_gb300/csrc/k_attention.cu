@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
       }
 #pragma unroll
       for (int h = 0; h < kMaxGroup; ++h)
-        if (h < g) SC[static_cast<size_t>(h) * c.slots + sid] = s[h];
+        if (h < g && ap.mass) SC[static_cast<size_t>(h) * c.slots + sid] = s[h];
     }
     // online softmax update of the tile, per head
 #pragma unroll
@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
     tok_lo = 0;
     tok_hi = n;
   }
+  if (!ap.mass) return;       // the policy ranks without the attention mass
   __syncthreads();
   // ---- attention mass of every token of the finished unit ----
   float* MS = c.mass + (static_cast<size_t>(lb) * c.Hkv + kvh) * c.slots;

@@ -331,7 +331,8 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   for (int mt = 0; mt < G::KS; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.0f;
   SoftState ss{-INFINITY, -INFINITY, 0.0f, 0.0f, 0.0f, 0.0f, 0};
   float* SC = c.scores + (static_cast<size_t>(lb) * c.Hq + kvh * g) * c.slots;
-  const bool wA = 2 * t4 < g, wB = 2 * t4 + 1 < g;
+  // raw scores are kept (for the mass epilogue) only when the policy uses them
+  const bool wA = ap.mass && 2 * t4 < g, wB = ap.mass && 2 * t4 + 1 < g;
 
   // one online-softmax update with a new scale exponent; returns 2^E
   auto update = [&](float mxA, float mxB, int Enew) -> float {
@@ -679,6 +680,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     }
     if (tid == 0) ap.ticket[unit] = 0u;
   }
+  if (!ap.mass) return;       // the policy ranks without the attention mass
   __syncthreads();
   // ---- attention mass of every token: sum over the group of p_{h,i} ----
   // Both regions start 16-byte aligned (cap8 % 32 == 0, slots % 16 == 0), so

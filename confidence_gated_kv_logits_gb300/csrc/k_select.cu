@@ -16,6 +16,9 @@
 //   key  = ema + 1/(1 + age)                       (fp32, one rounding per op)
 //   order: key descending, then position descending (newer wins a tie)
 //   protected: age < P (the new token included); append, then evict.
+// Comparison policies (same selection, compaction and storage): WINDOW key
+// 0 (the newest are kept), H2O acc = acc + a_i and key = acc, RANDOM key = a
+// SplitMix64 draw in [0, 1) per (step, sequence, token).
 // The fp32 operations use explicit _rn intrinsics so that no contraction
 // changes the rounding: the decision is taken in fp32 on exact fp32 values.
 //
@@ -30,6 +33,8 @@
 // INT8 quantisation of the aging token and the write of the new token.
 #include <cfloat>
 
+#include "../../include/confkv.h"
+
 #include "confkv_internal.cuh"
 
 namespace confkv {
@@ -38,6 +43,23 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kReg = 8;        // slots per thread held in registers (n <= 2048)
+
+// RANDOM policy: a uniform draw in [0, 1) per (step, sequence, token), the
+// top 24 bits of the SplitMix64 finaliser (Steele, Lea and Flood) chained
+// over (seed, t, l*B + b, position); exact in fp32.
+__device__ __forceinline__ uint64_t splitmix_mix(uint64_t x) {
+  x += 0x9E3779B97F4A7C15ull;
+  x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+  x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+  return x ^ (x >> 31);
+}
+__device__ __forceinline__ float random_key(uint64_t seed, int t, int lb, int pos) {
+  uint64_t h = splitmix_mix(seed);
+  h = splitmix_mix(h ^ static_cast<uint64_t>(static_cast<uint32_t>(t)));
+  h = splitmix_mix(h ^ static_cast<uint64_t>(static_cast<uint32_t>(lb)));
+  h = splitmix_mix(h ^ static_cast<uint64_t>(static_cast<uint32_t>(pos)));
+  return static_cast<float>(static_cast<uint32_t>(h >> 40)) * 0x1p-24f;
+}
 
 __device__ __forceinline__ unsigned long long key64(float key, int pos) {
   return (static_cast<unsigned long long>(__float_as_uint(key)) << 32) |
@@ -163,6 +185,7 @@ __device__ void quantize_row_warp(const __half* src, int8_t* dst, float* scale_o
   if (lane == 0) *scale_out = s;
 }
 
+template <int kPolicy>
 __global__ void __launch_bounds__(kThreads, 4) k_select(Cache c, StepParams sp) {
   const int lb = sp.lb0 + blockIdx.x;
   const int lbu = blockIdx.x;                 // index into the caller's buffers
@@ -207,6 +230,9 @@ __global__ void __launch_bounds__(kThreads, 4) k_select(Cache c, StepParams sp) 
   unsigned long long lmin = ~0ull;
   int lprot = 0;
   const float hqf = static_cast<float>(c.Hq);
+  // the EMA (CONF-KV) and the accumulated mass (H2O) read the previous
+  // attention's per-token mass; WINDOW and RANDOM rank without it
+  constexpr bool use_mass = kPolicy == CONFKV_POLICY_CONFKV || kPolicy == CONFKV_POLICY_H2O;
 for (int base = 0; base < ntok; base += kReg * kThreads) {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -220,14 +246,20 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
         const int j = is8 ? i : i - n8;
         sid[r] = (i < ntok) ? (is8 ? j : cap8 + j) : -1;
         pv[r] = (i < ntok) ? (is8 ? pos8[j] : pos16[j]) : 0;
-        ev[r] = (i < ntok) ? (is8 ? ema8[j] : ema16[j]) : 0.0f;
+        if constexpr (use_mass) {
+          ev[r] = (i < ntok) ? (is8 ? ema8[j] : ema16[j]) : 0.0f;
+        } else {
+          ev[r] = 0.0f;
+        }
         asum[r] = 0.0f;
       }
-      for (int h = 0; h < Hkv; ++h) {
-        const float* mh = mass + static_cast<size_t>(h) * c.slots;
+      if constexpr (use_mass) {
+        for (int h = 0; h < Hkv; ++h) {
+          const float* mh = mass + static_cast<size_t>(h) * c.slots;
 #pragma unroll
-        for (int r = 0; r < kH; ++r)
-          if (sid[r] >= 0) asum[r] = __fadd_rn(asum[r], mh[sid[r]]);
+          for (int r = 0; r < kH; ++r)
+            if (sid[r] >= 0) asum[r] = __fadd_rn(asum[r], mh[sid[r]]);
+        }
       }
 #pragma unroll
       for (int r = 0; r < kH; ++r) {
@@ -236,11 +268,22 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
         const int i = base + rr * kThreads + tid;
         const bool is8 = i < n8;
         const int j = is8 ? i : i - n8;
-        const float a = __fdiv_rn(asum[r], hqf);
-        const float e = __fadd_rn(__fmul_rn(sp.beta, ev[r]), __fmul_rn(sp.omb, a));
-        if (is8) ema8[j] = e; else ema16[j] = e;
         const int age = t - pv[r];
-        const float key = __fadd_rn(e, __fdiv_rn(1.0f, static_cast<float>(1 + age)));
+        float key;
+        if constexpr (kPolicy == CONFKV_POLICY_CONFKV) {
+          const float a = __fdiv_rn(asum[r], hqf);
+          const float e = __fadd_rn(__fmul_rn(sp.beta, ev[r]), __fmul_rn(sp.omb, a));
+          if (is8) ema8[j] = e; else ema16[j] = e;
+          key = __fadd_rn(e, __fdiv_rn(1.0f, static_cast<float>(1 + age)));
+        } else if constexpr (kPolicy == CONFKV_POLICY_H2O) {
+          const float e = __fadd_rn(ev[r], __fdiv_rn(asum[r], hqf));   // accumulated mass
+          if (is8) ema8[j] = e; else ema16[j] = e;
+          key = e;
+        } else if constexpr (kPolicy == CONFKV_POLICY_RANDOM) {
+          key = random_key(sp.seed, t, lb, pv[r]);
+        } else {
+          key = 0.0f;                                                   // WINDOW
+        }
         keys[sid[r]] = key;
         const bool prot = !is8 && age < P;
         if (prot) ++lprot;
@@ -262,7 +305,7 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
   // Every thread has read the previous attention's per-token mass, which this
   // step's attention rewrites for every live slot before the next read: drop
   // its whole 128-byte lines from L2 without a write-back.
-  {
+  if constexpr (use_mass) {
     const int l8 = n8 >> 5, l16 = n16 >> 5, per = l8 + l16;
     for (int x = tid; x < Hkv * per; x += kThreads) {
       const int h = x / per, r = x - h * per;
@@ -612,17 +655,33 @@ size_t select_smem_bytes(const Cache& c) {
          (static_cast<size_t>(c.Ncap) + 1 + c.Wr) * sizeof(int2);
 }
 
-cudaError_t launch_select(const Cache& c, const StepParams& sp, cudaStream_t s) {
-  const size_t smem = select_smem_bytes(c);
+namespace {
+
+template <int kPolicy>
+cudaError_t launch_select_p(const Cache& c, const StepParams& sp, size_t smem, cudaStream_t s) {
   static size_t attr = 48 * 1024;
   if (smem > attr) {
-    const cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(k_select<kPolicy>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr = smem;
   }
-  const cudaError_t e = launch_pdl(k_select, dim3(sp.nlb), dim3(kThreads), smem, s, c, sp);
+  const cudaError_t e = launch_pdl(k_select<kPolicy>, dim3(sp.nlb), dim3(kThreads), smem, s, c, sp);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_select(const Cache& c, const StepParams& sp, cudaStream_t s) {
+  const size_t smem = select_smem_bytes(c);
+  switch (sp.policy) {
+    case CONFKV_POLICY_CONFKV: return launch_select_p<CONFKV_POLICY_CONFKV>(c, sp, smem, s);
+    case CONFKV_POLICY_WINDOW: return launch_select_p<CONFKV_POLICY_WINDOW>(c, sp, smem, s);
+    case CONFKV_POLICY_H2O: return launch_select_p<CONFKV_POLICY_H2O>(c, sp, smem, s);
+    case CONFKV_POLICY_RANDOM: return launch_select_p<CONFKV_POLICY_RANDOM>(c, sp, smem, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace confkv

@@ -64,6 +64,33 @@ extern "C" {
 
 typedef struct confkv_ctx confkv_ctx;
 
+/*
+ * Ranking policies (confkv_opts.policy).  CONF-KV is the method; the others
+ * are the comparison points its pages name, run on the same cache, kernels
+ * and storage rule (tokens older than the newest W are INT8):
+ *   CONFKV  budget from the confidence; key = EMA mass + 1/(1 + age)
+ *                                                     [Tokenrangschikking]
+ *   WINDOW  fixed budget N_low, the newest tokens are kept (a sliding
+ *           window; with N_low and W at least the context length it is the
+ *           full FP16 cache).  No confidence is computed: conf_out and
+ *           budget_out are not written and logits may be NULL.
+ *   H2O     budget from the confidence; key = accumulated attention mass
+ *           (acc <- acc + a, fp32), the newest P protected: heavy hitters
+ *           plus a recent window
+ *   RANDOM  budget from the confidence; key = a uniform draw in [0, 1) per
+ *           (step, sequence, token): random eviction at CONF-KV's rate (the
+ *           pages' ablation).  The draw is the top 24 bits of SplitMix64
+ *           applied as h = mix(mix(mix(mix(seed) ^ t) ^ (l*B + b)) ^ pos),
+ *           with mix(x): x += 0x9E3779B97F4A7C15; x = (x ^ x>>30) *
+ *           0xBF58476D1CE4E5B9; x = (x ^ x>>27) * 0x94D049BB133111EB;
+ *           x ^ x>>31 (Steele, Lea and Flood's SplitMix64 finaliser).
+ * Ties between equal keys keep the newer position under every policy.
+ */
+#define CONFKV_POLICY_CONFKV 0
+#define CONFKV_POLICY_WINDOW 1
+#define CONFKV_POLICY_H2O 2
+#define CONFKV_POLICY_RANDOM 3
+
 /* Optional settings of confkv_create (all fields may be zero = default). */
 typedef struct confkv_opts {
   int batch;         /* B sequences decoded together (default 1) */
@@ -78,6 +105,9 @@ typedef struct confkv_opts {
                         cores, 2 tensor cores (requires Hq/Hkv <= 8) */
   int attn_tma;      /* tensor-core attention at head_dim 128 stages K/V tiles
                         with TMA (0, default) or with cp.async (-1) */
+  int policy;        /* CONFKV_POLICY_* (default CONFKV) */
+  int reserved;      /* must be 0 */
+  uint64_t seed;     /* RANDOM policy: seed of the draws */
 } confkv_opts;
 
 /* Counters read back by confkv_stats (cumulative since create unless noted). */

@@ -36,7 +36,10 @@ def build(force=False):
 class _Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("L", "B", "Hq", "Hkv", "d", "V", "N_low", "N_high", "P", "W")] + [
-        ("tau", ctypes.c_float), ("beta", ctypes.c_float), ("pyramid_min", ctypes.c_double)]
+        ("tau", ctypes.c_float), ("beta", ctypes.c_float), ("pyramid_min", ctypes.c_double),
+        ("policy", ctypes.c_int), ("reserved", ctypes.c_int), ("seed", ctypes.c_uint64)]
+
+POLICY_CONFKV, POLICY_WINDOW, POLICY_H2O, POLICY_RANDOM = 0, 1, 2, 3
 
 
 def _P(t):
@@ -61,6 +64,12 @@ def lib():
         L.orc_ema_update.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_float]
         L.orc_rank_key.restype = ctypes.c_float
         L.orc_rank_key.argtypes = [ctypes.c_float, ctypes.c_int64]
+        L.orc_h2o_update.restype = ctypes.c_float
+        L.orc_h2o_update.argtypes = [ctypes.c_float, ctypes.c_float]
+        L.orc_splitmix.restype = ctypes.c_uint64
+        L.orc_splitmix.argtypes = [ctypes.c_uint64]
+        L.orc_random_key.restype = ctypes.c_float
+        L.orc_random_key.argtypes = [ctypes.c_uint64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32]
         L.orc_select.restype = ctypes.c_int
         L.orc_select.argtypes = [ctypes.c_int, vp, vp, vp, ctypes.c_int, vp]
         L.orc_attention_head.restype = None
@@ -142,6 +151,20 @@ def rank_key(ema, age):
     return np.float32(lib().orc_rank_key(float(ema), int(age)))
 
 
+def h2o_update(acc, a):
+    return np.float32(lib().orc_h2o_update(float(acc), float(a)))
+
+
+def splitmix(x):
+    """SplitMix64 output function of the word x (the generator's output for
+    state x + golden gamma)."""
+    return int(lib().orc_splitmix(int(x) & (2**64 - 1)))
+
+
+def random_key(seed, t, lb, pos):
+    return np.float32(lib().orc_random_key(int(seed), int(t), int(lb), int(pos)))
+
+
 def select(key, pos, prot, N):
     key = _c(key, np.float32)
     pos = _c(pos, np.int32)
@@ -171,18 +194,20 @@ class Oracle:
     """The CONF-KV cache manager of every (layer, sequence), step by step."""
 
     def __init__(self, L, B, Hq, Hkv, d, V, N_low, N_high, tau, P, W, beta,
-                 pyramid_min=1.0):
+                 pyramid_min=1.0, policy=POLICY_CONFKV, seed=0):
         self.L, self.B, self.Hq, self.Hkv, self.d, self.V = L, B, Hq, Hkv, d, V
         self.N_low, self.N_high, self.P, self.W = N_low, N_high, P, W
-        prm = _Params(L, B, Hq, Hkv, d, V, N_low, N_high, P, W, tau, beta, pyramid_min)
+        self.policy = policy
+        prm = _Params(L, B, Hq, Hkv, d, V, N_low, N_high, P, W, tau, beta, pyramid_min,
+                      policy, 0, seed)
         self._h = lib().orc_create(ctypes.byref(prm))
         if not self._h:
             raise ValueError("oracle: invalid parameters")
 
     @classmethod
-    def for_workload(cls, w):
+    def for_workload(cls, w, policy=POLICY_CONFKV, seed=0):
         return cls(w.L, w.B, w.Hq, w.Hkv, w.d, w.V, w.N_low, w.N_high, w.tau, w.P,
-                   w.W, w.beta, w.pyramid_min)
+                   w.W, w.beta, w.pyramid_min, policy, seed)
 
     def __del__(self):
         h = getattr(self, "_h", None)

@@ -41,6 +41,17 @@
 //   * pyramid: N_l = max(P, floor(N*(1 - (1-pmin)*l/(L-1)) + 0.5))
 //   * prefill: no eviction; age >= W quantised; an optional last query seeds
 //     the attention mass, the EMA stays 0
+//
+// Comparison policies the pages name, on the same cache and storage rule
+// (the method's own budget, selection and compaction unless noted):
+//   * WINDOW: fixed budget N_low (per-layer factor applied), key 0, so the
+//     newest tokens are kept: the sliding-window baseline; with N_low and W at
+//     least the context length it is the full FP16 cache.  No EMA.
+//   * H2O: acc <- acc + a (fp32), key = acc: heavy hitters by accumulated
+//     attention mass, plus the protected recent window P.
+//   * RANDOM: key = a uniform draw in [0, 1) per (step, sequence, token): the
+//     top 24 bits of the SplitMix64 finaliser chained over
+//     (seed, t, l*B + b, position); random eviction at CONF-KV's rate.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -78,7 +89,11 @@ struct Params {
   int L, B, Hq, Hkv, d, V, N_low, N_high, P, W;
   float tau, beta;
   double pyramid_min;
+  int policy;
+  uint64_t seed;
 };
+
+enum { kConfKV = 0, kWindow = 1, kH2O = 2, kRandom = 3 };
 
 struct Tok {
   int32_t pos = 0;
@@ -116,6 +131,9 @@ struct orc_params {
   int L, B, Hq, Hkv, d, V, N_low, N_high, P, W;
   float tau, beta;
   double pyramid_min;
+  int policy;               // 0 CONF-KV, 1 WINDOW, 2 H2O, 3 RANDOM
+  int reserved;
+  uint64_t seed;            // RANDOM draws
 };
 
 // ---------------------------------------------------------------------------
@@ -203,6 +221,28 @@ float orc_rank_key(float ema, int64_t age) {
   return ema + r;
 }
 
+// H2O comparison: accumulated attention mass, fp32.
+float orc_h2o_update(float acc, float a) { return acc + a; }
+
+// RANDOM comparison: SplitMix64's output function (Steele, Lea and Flood,
+// "Fast splittable pseudorandom number generators", 2014), applied to
+// (seed, t, lb, pos) one word at a time; the top 24 bits of the result as a
+// fraction in [0, 1).
+uint64_t orc_splitmix(uint64_t x) {
+  x += 0x9E3779B97F4A7C15ull;
+  x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+  x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+  return x ^ (x >> 31);
+}
+
+float orc_random_key(uint64_t seed, int64_t t, int64_t lb, int32_t pos) {
+  uint64_t h = orc_splitmix(seed);
+  h = orc_splitmix(h ^ static_cast<uint64_t>(static_cast<uint32_t>(t)));
+  h = orc_splitmix(h ^ static_cast<uint64_t>(static_cast<uint32_t>(lb)));
+  h = orc_splitmix(h ^ static_cast<uint64_t>(static_cast<uint32_t>(pos)));
+  return static_cast<float>(h >> 40) / 16777216.0f;
+}
+
 // [Tokenrangschikking] keep every protected token and the best
 // (N - #protected) others by (key desc, pos desc).  keep[i] receives 0/1.
 // Returns the number of kept tokens.
@@ -253,11 +293,12 @@ orc_ctx* orc_create(const orc_params* prm) {
   if (!prm) return nullptr;
   const orc_params& q = *prm;
   if (q.L < 1 || q.B < 1 || q.Hkv < 1 || q.Hq < q.Hkv || q.Hq % q.Hkv || q.d < 1 ||
-      q.V < 2 || q.P < 1 || q.W < q.P || q.N_low < q.P || q.N_high < q.P)
+      q.V < 2 || q.P < 1 || q.W < q.P || q.N_low < q.P || q.N_high < q.P || q.policy < 0 ||
+      q.policy > 3)
     return nullptr;
   orc_ctx* c = new orc_ctx();
   c->p = Params{q.L, q.B, q.Hq, q.Hkv, q.d, q.V, q.N_low, q.N_high, q.P, q.W,
-                q.tau, q.beta, q.pyramid_min};
+                q.tau, q.beta, q.pyramid_min, q.policy, q.seed};
   c->lanes.resize(static_cast<size_t>(q.L) * q.B);
   c->active.assign(static_cast<size_t>(q.L) * q.B, 1);
   return c;
@@ -367,7 +408,7 @@ int orc_step(orc_ctx* c, const float* logits, const uint16_t* q, const uint16_t*
   for (int b = 0; b < p.B; ++b) {
     double comps[4];
     const double cb = orc_confidence(logits + static_cast<size_t>(b) * p.V, p.V, comps);
-    Nb[b] = orc_budget(cb, p.tau, p.N_low, p.N_high);
+    Nb[b] = (p.policy == kWindow) ? p.N_low : orc_budget(cb, p.tau, p.N_low, p.N_high);
     if (conf) conf[b] = cb;
     if (budget) budget[b] = Nb[b];
     if (flags) flags[b] = comps[3] != 0.0 ? 1 : 0;
@@ -377,8 +418,12 @@ int orc_step(orc_ctx* c, const float* logits, const uint16_t* q, const uint16_t*
       const size_t lb = static_cast<size_t>(l) * p.B + b;
       if (!c->active[lb]) continue;
       Lane& ln = c->lanes[lb];
-      // EMA update from the previous step's attention mass
-      for (Tok& tk : ln.toks) { tk.ema = orc_ema_update(tk.ema, tk.a_prev, p.beta); tk.a_prev = 0.0f; }
+      // EMA update (H2O: accumulation) from the previous step's attention mass
+      for (Tok& tk : ln.toks) {
+        if (p.policy == kConfKV) tk.ema = orc_ema_update(tk.ema, tk.a_prev, p.beta);
+        if (p.policy == kH2O) tk.ema = orc_h2o_update(tk.ema, tk.a_prev);
+        tk.a_prev = 0.0f;
+      }
       // append the new token (FP16, ema 0)
       Tok nt;
       nt.pos = static_cast<int32_t>(t);
@@ -391,7 +436,14 @@ int orc_step(orc_ctx* c, const float* logits, const uint16_t* q, const uint16_t*
       ln.key.resize(n); ln.key_pos.resize(n); ln.key_prot.resize(n);
       for (int i = 0; i < n; ++i) {
         const int64_t age = t - ln.toks[i].pos;
-        ln.key[i] = orc_rank_key(ln.toks[i].ema, age);
+        switch (p.policy) {
+          case kConfKV: ln.key[i] = orc_rank_key(ln.toks[i].ema, age); break;
+          case kH2O: ln.key[i] = ln.toks[i].ema; break;
+          case kRandom:
+            ln.key[i] = orc_random_key(p.seed, t, static_cast<int64_t>(lb), ln.toks[i].pos);
+            break;
+          default: ln.key[i] = 0.0f; break;     // WINDOW: the newest win the tie
+        }
         ln.key_pos[i] = ln.toks[i].pos;
         ln.key_prot[i] = age < p.P ? 1 : 0;
       }

@@ -76,7 +76,7 @@ def compare_cache(kv, orc, l, b, rep):
 
 
 def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, splits=0,
-        logits_override=None, kernel=0, tma=0, per_layer=False):
+        logits_override=None, kernel=0, tma=0, per_layer=False, policy=0, seed=0):
     """Run workload `w` on the GPU and in the oracle; return a Report.
 
     lbs: iterable of (l, b) the oracle simulates (default: all).
@@ -88,8 +88,9 @@ def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, spli
     dev = torch.device("cuda", 0)
     steps = w.steps if steps is None else steps
     kv = pkg.ConfKV.for_workload(w, device=0, attn_splits=splits, attn_kernel=kernel,
-                                attn_tma=tma)
-    orc = oracle.Oracle.for_workload(w)
+                                attn_tma=tma, policy=policy, seed=seed)
+    orc = oracle.Oracle.for_workload(w, policy, seed)
+    fixed_budget = policy == oracle.POLICY_WINDOW      # no confidence computed
     all_lbs = [(l, b) for l in range(w.L) for b in range(w.B)]
     lbs = all_lbs if lbs is None else list(lbs)
     mask = np.zeros((w.L, w.B), np.uint8)
@@ -150,7 +151,11 @@ def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, spli
         g_out, g_kp, g_kc = out.cpu().numpy(), kp.cpu().numpy(), kc.cpu().numpy()
         g_cf, g_bd = cf.cpu().numpy(), bd.cpu().numpy()
         t = w.position(s)
+        if fixed_budget:
+            g_bd = np.full(w.B, w.N_low, np.int32)
         for b in range(w.B):
+            if fixed_budget:
+                break
             rep.max_c_err = max(rep.max_c_err, abs(float(g_cf[b]) - r["conf"][b]))
             assert abs(float(g_cf[b]) - r["conf"][b]) < TOL_C, (s, b, g_cf[b], r["conf"][b])
             if g_bd[b] != r["budget"][b]:

@@ -216,3 +216,24 @@ def test_full_size_qwen32b_sampled():
     lbs = [(0, 0), (31, 5), (63, 7)]
     rep = _check(parity.run(w, steps=3, lbs=lbs, device_inputs=True, check_codes_every=2))
     assert rep.stats["tokens_evicted"] > 0
+
+
+# ---------------------------------------------------------------------------
+# comparison policies on the same kernels (WINDOW, H2O, RANDOM)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("policy", [1, 2, 3])
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 2, 128), (12, 12, 64)])
+def test_policies_parity(policy, Hq, Hkv, d):
+    w = small(L=2, B=3, Hq=Hq, Hkv=Hkv, d=d, prefill=90, steps=60, N_high=40, N_low=70,
+              P=8, W=20, V=64)
+    rep = _check(parity.run(w, policy=policy, seed=0xC0FFEE))
+    assert rep.stats["tokens_evicted"] > 0
+
+
+def test_window_full_kv_configuration():
+    # budget and FP16 window at least the context: nothing evicted, nothing
+    # quantised, attention over the full FP16 cache
+    w = small(L=2, B=2, prefill=100, steps=40, N_high=160, N_low=160, P=8, W=160, V=64)
+    rep = _check(parity.run(w, policy=1), min_frac=1.0)
+    assert rep.stats["tokens_evicted"] == 0 and rep.stats["tokens_quantized"] == 0
