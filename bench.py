@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-baselines", action="store_true",
+                   help="skip the full-KV and sliding-window comparison runs")
+    p.add_argument("--baseline-steps", type=int, default=32)
     p.add_argument("--layers", type=int, default=0,
                    help="profiling only: override the layer count (smaller capture)")
     p.add_argument("--step-bytes", action="store_true",
@@ -318,6 +321,64 @@ def run_reference(args):
     return 0
 
 
+def policy_step_time(w, policy, steps, warmup, dev):
+    """Decode-step time of the same workload under another ranking policy
+    (same kernels, inputs resident in HBM, CUDA events around the steps)."""
+    import torch
+
+    import confidence_gated_kv_logits_gb300 as pkg
+    from synth import device as sd
+    kv = pkg.ConfKV.for_workload(w, policy=policy)
+    if w.prefill:
+        Kp, Vp = sd.prefill_kv(w)
+        kv.prefill(Kp, Vp, w.prefill)
+        del Kp, Vp
+        torch.cuda.empty_cache()
+    S = steps + warmup
+    bufs = [sd.step_inputs(w, s) for s in range(S)]
+    out = torch.empty(w.L, w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+    kp = torch.empty(w.L, w.B, kv.Ncap, dtype=torch.int32, device=dev)
+    kc = torch.empty(w.L, w.B, dtype=torch.int32, device=dev)
+    for s in range(warmup):
+        kv.step(*bufs[s], out, kp, kc)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(warmup, S):
+        kv.step(*bufs[s], out, kp, kc)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    st, rc = kv.stats()
+    kv.close()
+    del bufs
+    torch.cuda.empty_cache()
+    return {"ms_per_step": ms, "tokens_per_s": w.B / (ms / 1e3), "cache_gb": st["cache_bytes"] / 1e9,
+            "status": rc}
+
+
+def baselines(w, confkv_ms, steps, warmup, dev):
+    """The pages' comparison points on this workload and these kernels:
+    full KV (no eviction, every token FP16) and a sliding window of CONF-KV's
+    own budget with the same FP16/INT8 storage rule."""
+    ctx = w.prefill + warmup + steps + 16
+    full = w.with_(N_low=ctx, N_high=ctx, W=ctx, name=f"{w.name}-full-kv")
+    cases = [("full_kv", full, "WINDOW policy, budget and FP16 window >= context: no eviction, "
+                               "no INT8")]
+    for n in sorted({w.N_low, w.N_high}, reverse=True):
+        cases.append((f"sliding_window_{n}", w.with_(N_low=n, N_high=n, name=f"{w.name}-window-{n}"),
+                      f"WINDOW policy, newest {n} tokens (one of CONF-KV's two budgets), FP16 "
+                      f"newest {w.W}, older INT8"))
+    r = {}
+    for key, wb, desc in cases:
+        m = policy_step_time(wb, 1, steps, warmup, dev)
+        m["what"] = desc
+        m["confkv_speedup"] = m["ms_per_step"] / confkv_ms
+        r[key] = m
+    return r
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -449,6 +510,10 @@ def run_ours(args):
         kv.close()
         del host_in
 
+    base = None
+    if ws == 1 and not args.no_baselines:
+        base = baselines(w, ms / K, args.baseline_steps, 3, dev)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)
@@ -471,10 +536,12 @@ def run_ours(args):
                          "achieved_gbs": pipe, "frac": pipe / hbm,
                          "attention_share_of_step": attn_ms / ms},
             "budget_high_fraction": hi_frac,
+            "mean_cached_tokens_per_lane": st1["cache_tokens"] / (w.L * w.B),
             "kernels_us": breakdown,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 4 * K,
+            "baselines": base,
+            "gpu_launches": 3 * K,
             "clocks": clocks.summary(wall0, wall1),
             "status": rc,
         }
