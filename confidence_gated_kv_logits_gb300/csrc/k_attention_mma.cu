@@ -39,6 +39,7 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;
+constexpr int kCorrEvery = 4;                   // INT8 chunks between V-offset corrections
 constexpr uint32_t kMagic = 0x64646464u;    // fp16 exponent byte of 1024
 constexpr uint32_t kH1152 = 0x64806480u;    // half2(1152, 1152)
 
@@ -284,8 +285,11 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   static_assert(!TMA || D == 128, "the TMA path is specialised for head_dim 128");
   constexpr int STAGE = TMA ? kTmaStage : G::STAGE;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  // 1024-byte aligned base (128-byte swizzle atoms)
-  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  // TMA path: 1024-byte aligned base for the 128-byte swizzle atoms (its
+  // launch allocates 1024 bytes of slack for this); the cp.async path needs
+  // 16-byte alignment only and has no slack, so it uses the base as is
+  unsigned char* smem =
+      TMA ? smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) : smem_raw;
   __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
   const int unit = ap.lb0 * c.Hkv + blockIdx.x, split = blockIdx.y;
   const int lb = unit / c.Hkv, kvh = unit - lb * c.Hkv, g = c.g;
@@ -394,6 +398,25 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       mma16816(O[mt], a, bh0, bh1);
       mma16816(O[mt], a, bl0, bl1);
     }
+  };
+
+  // Remove the 1152 * sum(P') that the offset V operand (1152 + code) added
+  // to every channel.  The tensor cores' fp32 accumulation rounds relative
+  // to the accumulator's magnitude, which the offset dominates, so the
+  // correction is applied every kCorrEvery INT8 chunks (and at the end):
+  // the accumulated offset, and with it the rounding, stays that of a few
+  // chunks instead of growing with the context.
+  auto remove_offset = [&]() {
+    const float oA = 1152.0f * gsum8(ss.spA), oB = 1152.0f * gsum8(ss.spB);
+#pragma unroll
+    for (int mt = 0; mt < G::KS; ++mt) {
+      O[mt][0] -= oA;
+      O[mt][2] -= oA;
+      O[mt][1] -= oB;
+      O[mt][3] -= oB;
+    }
+    ss.spA = 0.0f;
+    ss.spB = 0.0f;
   };
 
   // ---- main loop over this warp's chunks ----
@@ -516,6 +539,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
         }
         pv_int8(x, vw);
       }
+      if ((i & (kCorrEvery - 1)) == kCorrEvery - 1) remove_offset();
     } else {
       // ------------------------- FP16 chunk: 16 tokens -------------------------
       const int tb = 16 * (ci - nc8);
@@ -601,17 +625,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   // ---- merge the warps of this CTA (shared memory reused) ----
   ss.lA = gsum8(ss.lA);
   ss.lB = gsum8(ss.lB);
-  {
-    // remove the 1152 * sum(P') the offset V operand added to every channel
-    const float oA = 1152.0f * gsum8(ss.spA), oB = 1152.0f * gsum8(ss.spB);
-#pragma unroll
-    for (int mt = 0; mt < G::KS; ++mt) {
-      O[mt][0] -= oA;
-      O[mt][2] -= oA;
-      O[mt][1] -= oB;
-      O[mt][3] -= oB;
-    }
-  }
+  remove_offset();
   __syncthreads();
   float* wm = reinterpret_cast<float*>(smem);            // [kWarps][8]
   float* wl = wm + kWarps * 8;                           // [kWarps][8]

@@ -166,6 +166,25 @@ def q_last_lb(w, l, b):
     return None if q is None else q[l, b]
 
 
+def step_inputs_lanes(w, s, lbs):
+    """Inputs of decode step s with q / k_new / v_new filled for the (l, b)
+    lanes in `lbs` only (other lanes zero) and the full logits."""
+    lg = step_logits(w, s)
+    q = np.zeros((w.L, w.B, w.Hq, w.d), np.float16)
+    k = np.zeros((w.L, w.B, w.Hkv, w.d), np.float16)
+    v = np.zeros((w.L, w.B, w.Hkv, w.d), np.float16)
+    nq, nk = w.Hq * w.d, w.Hkv * w.d
+    for l, b in lbs:
+        lb = l * w.B + b
+        q[l, b] = gen.gen_f16(w.seed, gen.KIND_Q, s, q.shape, lb * nq, (lb + 1) * nq).reshape(
+            w.Hq, w.d)
+        k[l, b] = gen.gen_f16(w.seed, gen.KIND_KNEW, s, k.shape, lb * nk, (lb + 1) * nk,
+                              heavy=True, inner=w.d, tlen=1, pos0=w.position(s)).reshape(w.Hkv, w.d)
+        v[l, b] = gen.gen_f16(w.seed, gen.KIND_VNEW, s, v.shape, lb * nk, (lb + 1) * nk).reshape(
+            w.Hkv, w.d)
+    return lg, q, k, v
+
+
 def step_inputs_lane(w, s, l, b):
     """Inputs of decode step s with q / k_new / v_new filled for (l, b) only
     (other lanes zero) and the full logits: enough for an oracle that

@@ -127,7 +127,10 @@ def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, spli
     diverged = set()
     prev = {}
     for s in range(steps):
-        lg, q, k, v = wl.step_inputs(w, s)
+        if device_inputs and lbs is not all_lbs:
+            lg, q, k, v = wl.step_inputs_lanes(w, s, lbs)     # host inputs of the sampled lanes
+        else:
+            lg, q, k, v = wl.step_inputs(w, s)
         if logits_override is not None:
             lg = logits_override(s, lg)
         if device_inputs and logits_override is None:
