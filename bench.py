@@ -526,7 +526,8 @@ def run_ours(args):
             "dtype": "f32 (fp16 + int8 KV storage, fp32 accumulate)", "data": "synthetic",
             "config": workload_config(w, {"parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
                                           "decode_steps": S}),
-            "roofline": {"bound": "hbm", "kernel": "attention (k_attn_mma, TMA)",
+            "roofline": {"bound": "hbm",
+                         "kernel": "attention (k_attn_mma, %s)" % ("TMA" if w.d == 128 else "cp.async"),
                          "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_kind": f"{peak_kind} HBM copy",
                          "traffic": attention_traffic(),
