@@ -36,8 +36,11 @@
  *     and returned by the next confkv_stats() call.  No exception crosses the
  *     ABI; no call traps the GPU.
  *   - confkv_step never synchronises the host with the GPU and allocates
- *     nothing, so a sequence of steps can be captured in a CUDA graph once
- *     the context exists.
+ *     nothing, so steps can be captured in a CUDA graph once the context
+ *     exists.  The step's position is a launch parameter taken from the
+ *     host-side counter, which advances at capture time: a captured graph
+ *     replays exactly the steps it recorded, once, and must not be replayed
+ *     again (capture anew for the next steps).
  */
 #ifndef CONFKV_H_
 #define CONFKV_H_

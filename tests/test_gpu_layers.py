@@ -97,3 +97,39 @@ def test_per_layer_state_errors():
     st, rc = kv.stats()
     assert rc == 0 and st["steps"] == 1 and st["position"] == 1     # no prefill here
     kv.close()
+
+
+def test_step_captured_in_cuda_graph_equals_eager():
+    # a step captured in a CUDA graph (allocation-free, no host sync) and
+    # replayed once gives the same bits as the same step run eagerly
+    import confidence_gated_kv_logits_gb300 as pkg
+    w = small(L=2, B=2, steps=12)
+    outs = []
+    for graph in (False, True):
+        kv = pkg.ConfKV.for_workload(w, device=0)
+        out = torch.zeros(w.L, w.B, w.Hq, w.d, device=DEV)
+        kp = torch.full((w.L, w.B, kv.Ncap), -1, dtype=torch.int32, device=DEV)
+        kc = torch.zeros(w.L, w.B, dtype=torch.int32, device=DEV)
+        inputs = [tuple(torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+                        for x in wl.step_inputs(w, s)) for s in range(w.steps)]
+        torch.cuda.synchronize()
+        for s in range(w.steps - 1):
+            kv.step(*inputs[s], out, kp, kc)
+        last = inputs[-1]
+        if graph:
+            stream = torch.cuda.Stream()
+            stream.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                kv.step(*last, out, kp, kc, stream=stream)
+            g.replay()
+        else:
+            kv.step(*last, out, kp, kc)
+        torch.cuda.synchronize()
+        st, rc = kv.stats()
+        assert rc == 0 and st["steps"] == w.steps
+        outs.append((out.cpu().numpy(), kp.cpu().numpy(), kc.cpu().numpy()))
+        kv.close()
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a.view(np.uint32) if a.dtype == np.float32 else a,
+                              b.view(np.uint32) if b.dtype == np.float32 else b)
