@@ -269,7 +269,7 @@ class ConfKV:
         r["n8"], r["n16"] = a, c
         return r
 
-    KERNELS = ("confidence", "select", "compact", "attention")
+    KERNELS = ("confidence", "select", "append", "attention")
 
     def profile(self, kernels=()):
         """Time the named kernels with CUDA events (empty: off)."""

@@ -26,7 +26,7 @@ constexpr int kSmCount = 152;
 constexpr int kProfKernels = 4;
 // "select" covers ranking, eviction, compaction moves and INT8 aging; slot 2
 // is unused (kept so that the kernel mask bits stay stable).
-const char* const kProfNames[kProfKernels] = {"confidence", "select", "unused", "attention"};
+const char* const kProfNames[kProfKernels] = {"confidence", "select", "append", "attention"};
 
 struct DeviceGuard {
   int prev = -1;
@@ -52,7 +52,9 @@ struct confkv_ctx {
   float tau = 0.f, beta = 0.f, omb = 0.f, pyramid_min = 1.f;
   int policy = CONFKV_POLICY_CONFKV;
   uint64_t seed = 0;
-  int64_t t = 0, steps = 0;
+  int64_t t = 0, steps = 0;   // host view: steps launched eagerly (a replayed
+                              // graph advances only the device counters)
+  int64_t t0 = 0;             // prefill length
   bool prefilled = false;
   Cache cache{};
   float* conf = nullptr;
@@ -153,9 +155,23 @@ int auto_splits(int units, int ncap) {
   return std::max(1, std::min(std::min(want, tok_lim), 16));
 }
 
+// One layer's launch holds few units, so its time is one CTA's latency: about
+// two CTAs per SM in a single wave, at most one cluster (8 splits) per unit.
+int auto_splits_layer(int units, int ncap) {
+  const int want = std::max(1, 2 * kSmCount / units);
+  const int tok_lim = std::max(1, (ncap + 1 + 127) / 128);
+  return std::max(1, std::min(std::min(want, tok_lim), 8));
+}
+
 int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s, int lb0, int nlb,
-                  int splits) {
+                  int splits, const StepParams* fused = nullptr) {
   AttnParams ap{};
+  if (fused) {
+    ap.k_new = fused->k_new;
+    ap.v_new = fused->v_new;
+    ap.kept_pos = fused->kept_pos;
+    ap.kept_count = fused->kept_count;
+  }
   ap.lb0 = lb0;
   ap.nlb = nlb;
   ap.q = q;
@@ -237,7 +253,7 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
     c->splits = c->splits_layer = o.attn_splits;
   } else {
     c->splits = auto_splits(units, c->Ncap);
-    c->splits_layer = auto_splits(c->B * c->Hkv, c->Ncap);
+    c->splits_layer = auto_splits_layer(c->B * c->Hkv, c->Ncap);
   }
   const int max_splits = std::max(c->splits, c->splits_layer);
 
@@ -261,6 +277,8 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   A(dalloc(c, &k.keys, LB * c->slots));
   A(dalloc(c, &k.n8, LB));
   A(dalloc(c, &k.n16, LB));
+  A(dalloc(c, &k.new_slot, LB));
+  A(dalloc(c, &k.tstep, LB));
   A(dalloc(c, &k.stats, 1));
   A(dalloc(c, &k.err, 1));
   A(dalloc(c, &c->conf, c->B));
@@ -309,6 +327,7 @@ int confkv_prefill(confkv_ctx* c, const uint16_t* k, const uint16_t* v, int T,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   c->prefilled = true;
   c->t = T;
+  c->t0 = T;
   if (T == 0) return CONFKV_OK;
   cudaError_t e = confkv::launch_prefill_store(c->cache, reinterpret_cast<const __half*>(k),
                                                reinterpret_cast<const __half*>(v), T, s);
@@ -340,7 +359,6 @@ int run_confidence(confkv_ctx* c, const float* logits, float* conf_out, int32_t*
                    cudaStream_t s) {
   if (reinterpret_cast<uintptr_t>(logits) & 3u)
     return fail(c, CONFKV_ERR_INVALID_ARG, "misaligned logits");
-  if (c->t >= 0x7fffffffLL) return fail(c, CONFKV_ERR_STATE, "position overflow");
   prof_mark(c, 0, s);
   const cudaError_t e = confkv::launch_confidence(
       logits, c->B, c->V, c->tau, c->N_low, c->N_high, c->conf, c->hi, conf_out, budget_out,
@@ -350,14 +368,12 @@ int run_confidence(confkv_ctx* c, const float* logits, float* conf_out, int32_t*
   return CONFKV_OK;
 }
 
-// selection + compaction + attention of the (layer, sequence) range [lb0, lb0 + nlb)
-int run_layers(confkv_ctx* c, int lb0, int nlb, int splits, const uint16_t* q,
-               const uint16_t* k_new, const uint16_t* v_new, float* out, int32_t* kept_pos,
-               int32_t* kept_count, cudaStream_t s) {
+StepParams step_params(const confkv_ctx* c, int lb0, int nlb, const uint16_t* k_new,
+                       const uint16_t* v_new, int32_t* kept_pos, int32_t* kept_count) {
   StepParams sp{};
   sp.lb0 = lb0;
   sp.nlb = nlb;
-  sp.t = static_cast<int>(c->t);
+  sp.t0 = static_cast<int>(c->t0);
   sp.beta = c->beta;
   sp.omb = c->omb;
   sp.btab = c->btab;
@@ -368,12 +384,21 @@ int run_layers(confkv_ctx* c, int lb0, int nlb, int splits, const uint16_t* q,
   sp.v_new = reinterpret_cast<const __half*>(v_new);
   sp.policy = c->policy;
   sp.seed = c->seed;
+  return sp;
+}
+
+int run_select(confkv_ctx* c, const StepParams& sp, cudaStream_t s) {
   prof_mark(c, 1, s);
   const cudaError_t e = confkv::launch_select(c->cache, sp, s);
   prof_mark(c, 1, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("select: ") + cudaGetErrorString(e));
+  return CONFKV_OK;
+}
+
+int run_attention_timed(confkv_ctx* c, const uint16_t* q, float* out, cudaStream_t s, int lb0,
+                        int nlb, int splits, const StepParams* fused = nullptr) {
   prof_mark(c, 3, s);
-  const int rc = run_attention(c, reinterpret_cast<const __half*>(q), out, s, lb0, nlb, splits);
+  const int rc = run_attention(c, reinterpret_cast<const __half*>(q), out, s, lb0, nlb, splits, fused);
   prof_mark(c, 3, s);
   return rc;
 }
@@ -390,13 +415,16 @@ int confkv_step(confkv_ctx* c, const float* logits, const uint16_t* q, const uin
   int rc = check_layer_args(c, q, k_new, v_new, out);
   if (rc != CONFKV_OK) return rc;
   if (c->step_open) return fail(c, CONFKV_ERR_STATE, "a per-layer step is open");
+  if (c->t >= 0x7fffffffLL) return fail(c, CONFKV_ERR_STATE, "position overflow");
   DeviceGuard guard(c->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (uses_confidence(c)) {
     rc = run_confidence(c, logits, conf_out, budget_out, s);
     if (rc != CONFKV_OK) return rc;
   }
-  rc = run_layers(c, 0, c->L * c->B, c->splits, q, k_new, v_new, out, kept_pos, kept_count, s);
+  rc = run_select(c, step_params(c, 0, c->L * c->B, k_new, v_new, kept_pos, kept_count), s);
+  if (rc != CONFKV_OK) return rc;
+  rc = run_attention_timed(c, q, out, s, 0, c->L * c->B, c->splits);
   if (rc != CONFKV_OK) return rc;
   c->t += 1;
   c->steps += 1;
@@ -408,11 +436,19 @@ int confkv_step_begin(confkv_ctx* c, const float* logits, float* conf_out, int32
   if (!c) return CONFKV_ERR_INVALID_ARG;
   if (!logits && uses_confidence(c)) return fail(c, CONFKV_ERR_INVALID_ARG, "null logits");
   if (c->step_open) return fail(c, CONFKV_ERR_STATE, "the previous step still has layers to run");
+  if (c->t >= 0x7fffffffLL) return fail(c, CONFKV_ERR_STATE, "position overflow");
   DeviceGuard guard(c->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (uses_confidence(c)) {
-    const int rc = run_confidence(c, logits, conf_out, budget_out, static_cast<cudaStream_t>(stream));
+    const int rc = run_confidence(c, logits, conf_out, budget_out, s);
     if (rc != CONFKV_OK) return rc;
   }
+  // the selection of every layer needs nothing of this step but the budgets:
+  // it runs here in one launch and reserves each arriving token's FP16 slot
+  StepParams sp = step_params(c, 0, c->L * c->B, nullptr, nullptr, nullptr, nullptr);
+  sp.defer_new = 1;
+  const int rc = run_select(c, sp, s);
+  if (rc != CONFKV_OK) return rc;
   c->step_open = true;
   c->layers_left = c->L;
   std::fill(c->layer_done.begin(), c->layer_done.end(), 0);
@@ -429,8 +465,18 @@ int confkv_step_layer(confkv_ctx* c, int layer, const uint16_t* q, const uint16_
   if (!c->step_open) return fail(c, CONFKV_ERR_STATE, "no step begun (confkv_step_begin)");
   if (c->layer_done[layer]) return fail(c, CONFKV_ERR_STATE, "layer already run in this step");
   DeviceGuard guard(c->device);
-  rc = run_layers(c, layer * c->B, c->B, c->splits_layer, q, k_new, v_new, out, kept_pos,
-                  kept_count, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const StepParams sp = step_params(c, layer * c->B, c->B, k_new, v_new, kept_pos, kept_count);
+  // the tensor-core attention stores the arriving token itself; the CUDA-core
+  // one runs after a separate append launch
+  const bool fused = confkv::attention_uses_mma(c->cache, c->attn_kernel);
+  if (!fused) {
+    prof_mark(c, 2, s);
+    const cudaError_t e = confkv::launch_append(c->cache, sp, s);
+    prof_mark(c, 2, s);
+    if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("append: ") + cudaGetErrorString(e));
+  }
+  rc = run_attention_timed(c, q, out, s, layer * c->B, c->B, c->splits_layer, fused ? &sp : nullptr);
   if (rc != CONFKV_OK) return rc;
   c->layer_done[layer] = 1;
   if (--c->layers_left == 0) {
@@ -502,11 +548,13 @@ int confkv_stats(confkv_ctx* c, confkv_stats_t* out) {
   if (e == cudaSuccess) e = cudaMemcpy(&err, c->cache.err, sizeof(err), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemcpy(n8.data(), c->cache.n8, LB * 4, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemcpy(n16.data(), c->cache.n16, LB * 4, cudaMemcpyDeviceToHost);
+  int32_t tstep0 = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&tstep0, c->cache.tstep, 4, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(c->cache.err, 0, sizeof(int32_t));
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("stats: ") + cudaGetErrorString(e));
   std::memset(out, 0, sizeof(*out));
-  out->steps = c->steps;
-  out->position = c->t;
+  out->steps = static_cast<int64_t>(ds.steps);
+  out->position = c->t0 + tstep0;
   out->error_flags = err;
   out->tokens_evicted = static_cast<int64_t>(ds.evicted);
   out->tokens_quantized = static_cast<int64_t>(ds.quantized);

@@ -71,6 +71,7 @@ struct DevStats {
   unsigned long long kv_bytes;
   unsigned long long logits_bytes;
   unsigned long long hi_steps;
+  unsigned long long steps;   // decode steps whose selection has run
 };
 
 struct ConfPart {       // partial confidence state of one CTA
@@ -95,6 +96,11 @@ struct Cache {
   float* keys;      // [L*B][slots] ranking keys of the current step
   int32_t* n8;
   int32_t* n16;
+  int32_t* tstep;     // [L*B] decode steps run since the prefill; the arriving
+                      // token's position is t0 + tstep (kept on the device so
+                      // that a captured step can be replayed)
+  int32_t* new_slot;  // [L*B] FP16 slot reserved for the arriving token when the
+                      // selection runs ahead of the layer's K/V (per-layer steps)
   DevStats* stats;
   int32_t* err;
 };
@@ -102,7 +108,7 @@ struct Cache {
 struct StepParams {
   int lb0, nlb;          // (layer, sequence) range of this launch: [lb0, lb0 + nlb);
                          // the caller's buffers below start at lb0
-  int t;                 // position of the new token
+  int t0;                // prefill length: position of the first decoded token
   float beta, omb;       // EMA decay and 1 - decay (fp32)
   const int32_t* btab;   // [L][2] per-layer budget for (N_low, N_high)
   const int32_t* hi;     // [B] 1 if the sequence chose N_high
@@ -111,6 +117,8 @@ struct StepParams {
   const __half* k_new;   // [L*B][Hkv][d] key / value of the new token
   const __half* v_new;
   int policy;            // CONFKV_POLICY_*: ranking key and EMA rule
+  int defer_new;         // 1: reserve the arriving token's FP16 slot in new_slot and
+                         // leave its K/V rows and the kept lists to launch_append
   uint64_t seed;         // RANDOM policy draws
 };
 
@@ -126,6 +134,15 @@ struct AttnParams {
   unsigned int* ticket;  // [L*B*Hkv]
   float scale;           // 1/sqrt(d)
   int mass;              // 1: write the per-token attention mass (EMA / H2O policies)
+  int cluster;           // set by the launcher: the splits of a unit are one cluster
+  // Per-layer steps on the tensor-core path (else null): the arriving token's
+  // K/V [nlb][Hkv][d], stored into the FP16 slot the selection reserved
+  // (new_slot) before that slot is read, and the kept positions [nlb][Ncap] /
+  // counts [nlb] of the range (either may be null).
+  const __half* k_new;
+  const __half* v_new;
+  int32_t* kept_pos;
+  int32_t* kept_count;
 };
 
 // ---- launch wrappers (each file owns its kernels) ----
@@ -135,9 +152,16 @@ cudaError_t launch_confidence(const float* logits, int B, int V, float tau, int 
                               int32_t* budget_out, int32_t* err, DevStats* st, ConfPart* part,
                               unsigned int* ticket, cudaStream_t s);
 cudaError_t launch_select(const Cache& c, const StepParams& sp, cudaStream_t s);
+// Second half of a deferred selection for (layer, sequence) range [lb0, lb0 + nlb):
+// stores the arriving token's K/V rows (k_new, v_new) in the reserved FP16
+// slots and writes kept_pos / kept_count when given.
+cudaError_t launch_append(const Cache& c, const StepParams& sp, cudaStream_t s);
 cudaError_t launch_prefill_store(const Cache& c, const __half* k, const __half* v, int T,
                                  cudaStream_t s);
 cudaError_t launch_attention(const Cache& c, const AttnParams& ap, cudaStream_t s);
+// true if launch_attention runs the tensor-core kernel for this cache and
+// AttnParams::kernel (only that kernel handles AttnParams::k_new)
+bool attention_uses_mma(const Cache& c, int kernel);
 cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStream_t s);
 // Encodes the four tensor maps of the d = 128 TMA attention path into `out`
 // (kTmaMapsBytes bytes, 64-byte aligned); returns false if the driver cannot

@@ -256,10 +256,15 @@ cudaError_t launch_simple(const Cache& c, const AttnParams& ap, cudaStream_t s) 
 
 }  // namespace
 
+bool attention_uses_mma(const Cache& c, int kernel) {
+  return kernel != 1 && c.g >= 1 && c.g <= 8;
+}
+
 cudaError_t launch_attention(const Cache& c, const AttnParams& ap, cudaStream_t s) {
   const bool mma_ok = c.g >= 1 && c.g <= 8;
   if (ap.kernel == 2 && !mma_ok) return cudaErrorInvalidValue;
-  if (ap.kernel != 1 && mma_ok) return launch_attention_mma(c, ap, s);
+  if (attention_uses_mma(c, ap.kernel)) return launch_attention_mma(c, ap, s);
+  if (ap.k_new || ap.kept_pos || ap.kept_count) return cudaErrorInvalidValue;
   if (c.d == 64) return launch_simple<64>(c, ap, s);
   if (c.d == 128) return launch_simple<128>(c, ap, s);
   return cudaErrorInvalidValue;

@@ -26,6 +26,14 @@
 // tokens, 8 KB at d = 128) through a cp.async ring of kStages stages in a
 // thread-private shared-memory layout (conflict-free, no cross-lane data
 // except the 64 scales of an INT8 chunk).
+//
+// Split-K: with 2..8 splits the splits of a unit form one thread-block
+// cluster and merge through distributed shared memory: after a cluster
+// barrier every CTA reads the others' (max, sum) per head, computes its share
+// of the output from their partial accumulators and the attention mass of its
+// own tokens.  With more splits the partials go through global memory and the
+// CTA taking the last ticket finishes the unit.
+#include <cooperative_groups.h>
 #include <cuda.h>
 
 #include <cfloat>
@@ -39,6 +47,7 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;
+constexpr int kMaxClusterSplits = 8;            // portable cluster size
 constexpr int kCorrEvery = 4;                   // INT8 chunks between V-offset corrections
 constexpr uint32_t kMagic = 0x64646464u;    // fp16 exponent byte of 1024
 constexpr uint32_t kH1152 = 0x64806480u;    // half2(1152, 1152)
@@ -321,6 +330,27 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   const int ce = static_cast<int>(static_cast<long long>(nc) * (split + 1) / ap.splits);
   const int cnt = (ce - cb > warp) ? (ce - cb - warp + kWarps - 1) / kWarps : 0;
   const uint32_t wbase = smem_u32(smem) + warp * kStages * STAGE;
+  // Per-layer steps: the selection ran ahead and reserved FP16 slot hn for the
+  // arriving token.  The one CTA whose chunk range holds that slot stores the
+  // token's K/V rows of this KV head before any of its tiles is read.
+  if (ap.k_new) {
+    const int hn = c.new_slot[lb];
+    const int cf = nc8 + (hn >> 4);
+    if (cf >= cb && cf < ce) {
+      const size_t src = (static_cast<size_t>(lbu) * c.Hkv + kvh) * D;
+      const size_t dst = (static_cast<size_t>(unit) * c.Wr + hn) * D;
+      for (int it = tid; it < D / 4; it += kThreads) {     // D/8 16-byte pieces of K, then V
+        const bool isv = it >= D / 8;
+        const int ch = isv ? it - D / 8 : it;
+        reinterpret_cast<int4*>((isv ? c.v16 : c.k16) + dst)[ch] =
+            reinterpret_cast<const int4*>((isv ? ap.v_new : ap.k_new) + src)[ch];
+      }
+      // the tiles are read by TMA (the async proxy): order the generic stores first
+      if constexpr (TMA) asm volatile("fence.proxy.async.global;\n" ::: "memory");
+      __syncthreads();
+      if constexpr (TMA) asm volatile("fence.proxy.async.global;\n" ::: "memory");
+    }
+  }
   if constexpr (TMA) {
     if (lane == 0)
       for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
@@ -614,6 +644,17 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   }
   if constexpr (!TMA) cp_wait<0>();
   pdl_trigger();     // the next kernel in the stream may be scheduled
+  if (split == 0 && kvh == 0) {
+    // per-layer steps: the kept positions of this (layer, sequence), INT8
+    // slots then FP16 slots
+    if (ap.kept_pos) {
+      const int32_t* pos8 = c.pos8 + static_cast<size_t>(lb) * c.cap8;
+      const int32_t* pos16 = c.pos16 + static_cast<size_t>(lb) * c.Wr;
+      int32_t* kp = ap.kept_pos + static_cast<size_t>(lbu) * c.Ncap;
+      for (int i = tid; i < n8 + n16; i += kThreads) kp[i] = (i < n8) ? pos8[i] : pos16[i - n8];
+    }
+    if (ap.kept_count && tid == 0) ap.kept_count[lbu] = n8 + n16;
+  }
   if (!ok_all) {
     // a tile never arrived: flag the step (its output for this unit is
     // incomplete) and give the copy in flight one more bounded wait before
@@ -631,6 +672,8 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   float* wl = wm + kWarps * 8;                           // [kWarps][8]
   float* fin = wl + kWarps * 8;                          // [2][8]
   float* wo = fin + 16;                                  // [kWarps][8][D]
+  float* cml = wo + kWarps * 8 * D;                      // cluster: this split's [2][8] max, sum
+  float* cacc = cml + 16;                                // cluster: this split's [8][D] output
   const float unscale = pow2i(-ss.E);
   if (gid == 0) {
     wm[warp * 8 + 2 * t4] = ss.mA;
@@ -664,13 +707,52 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     if (ap.splits == 1) {
       outp[h * D + dd] = A / Ls;
       if (dd == 0) { fin[h] = M; fin[8 + h] = Ls; }
+    } else if (ap.cluster) {
+      cacc[h * D + dd] = A;
+      if (dd == 0) { cml[h] = M; cml[8 + h] = Ls; }
     } else {
       const size_t pi = (obase + h) * ap.splits + split;
       ap.part_acc[pi * D + dd] = A;
       if (dd == 0) { ap.part_ml[pi * 2] = M; ap.part_ml[pi * 2 + 1] = Ls; }
     }
   }
-  if (ap.splits > 1) {
+  if (ap.cluster) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int S = ap.splits;                // the cluster's CTAs; this one is rank `split`
+    cluster.sync();                         // every split's partial is in its shared memory
+    float* pm = wo;                         // [g][S] max, then rescale weight
+    float* pl = wo + 8 * 64;                // [g][S] sum
+    for (int x = tid; x < g * S; x += kThreads) {
+      const int h = x / S, sp = x - h * S;
+      const float* r = cluster.map_shared_rank(cml, sp);
+      pm[x] = r[h];
+      pl[x] = r[8 + h];
+    }
+    __syncthreads();
+    if (tid < g) {
+      float M = -INFINITY, Ls = 0.0f;
+      for (int sp = 0; sp < S; ++sp) M = fmaxf(M, pm[tid * S + sp]);
+      for (int sp = 0; sp < S; ++sp) {
+        const float f = rescale(pm[tid * S + sp], M);
+        Ls += pl[tid * S + sp] * f;
+        pm[tid * S + sp] = f;
+      }
+      fin[tid] = M;
+      fin[8 + tid] = Ls;
+    }
+    __syncthreads();
+    // this split's share of the output: blocks of kThreads elements, dealt
+    // round-robin over the splits
+    for (int idx = split * kThreads + tid; idx < g * D; idx += S * kThreads) {
+      const int h = idx / D, dd = idx - h * D;
+      float A = 0.0f;
+      for (int sp = 0; sp < S; ++sp)
+        A += cluster.map_shared_rank(cacc, sp)[h * D + dd] * pm[h * S + sp];
+      outp[h * D + dd] = A / fin[8 + h];
+    }
+    cluster.sync();                         // no CTA leaves while its partial may be read
+  } else if (ap.splits > 1) {
     __shared__ int s_last;
     __threadfence();
     __syncthreads();
@@ -678,19 +760,52 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    for (int idx = tid; idx < g * D; idx += kThreads) {
-      const int h = idx / D, dd = idx - h * D;
-      const size_t pb = (obase + h) * ap.splits;
-      float M = -INFINITY;
-      for (int sp = 0; sp < ap.splits; ++sp) M = fmaxf(M, __ldcg(&ap.part_ml[(pb + sp) * 2]));
-      float Ls = 0.0f, A = 0.0f;
-      for (int sp = 0; sp < ap.splits; ++sp) {
-        const float f = rescale(__ldcg(&ap.part_ml[(pb + sp) * 2]), M);
-        Ls += __ldcg(&ap.part_ml[(pb + sp) * 2 + 1]) * f;
-        A += __ldcg(&ap.part_acc[(pb + sp) * D + dd]) * f;
+    // every split's (max, sum) of each head once, into shared memory (the
+    // warp-merge area is free again)
+    float* pm = wo;                         // [g][splits] max, then rescale weight
+    float* pl = wo + 8 * 64;                // [g][splits] sum
+    const int S = ap.splits;
+    for (int x = tid; x < g * S; x += kThreads) {
+      const size_t pi = (obase + x / S) * S + x % S;
+      pm[x] = __ldcg(&ap.part_ml[pi * 2]);
+      pl[x] = __ldcg(&ap.part_ml[pi * 2 + 1]);
+    }
+    __syncthreads();
+    if (tid < g) {
+      float M = -INFINITY, Ls = 0.0f;
+      for (int sp = 0; sp < S; ++sp) M = fmaxf(M, pm[tid * S + sp]);
+      for (int sp = 0; sp < S; ++sp) {
+        const float f = rescale(pm[tid * S + sp], M);
+        Ls += pl[tid * S + sp] * f;
+        pm[tid * S + sp] = f;
       }
-      outp[h * D + dd] = A / Ls;
-      if (dd == 0) { fin[h] = M; fin[8 + h] = Ls; }
+      fin[tid] = M;
+      fin[8 + tid] = Ls;
+    }
+    __syncthreads();
+    // the weighted sum of the partial outputs: each thread's (at most
+    // 8 * D / kThreads) elements load together, split after split
+    constexpr int kPer = 8 * D / kThreads;
+    float A[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) A[k] = 0.0f;
+    for (int sp = 0; sp < S; ++sp) {
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = tid + k * kThreads;
+        if (idx < g * D) {
+          const int h = idx / D, dd = idx - h * D;
+          A[k] += __ldcg(&ap.part_acc[((obase + h) * S + sp) * D + dd]) * pm[h * S + sp];
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = tid + k * kThreads;
+      if (idx < g * D) {
+        const int h = idx / D, dd = idx - h * D;
+        outp[h * D + dd] = A[k] / fin[8 + h];
+      }
     }
     if (tid == 0) ap.ticket[unit] = 0u;
   }
@@ -707,38 +822,61 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   }
   float* MS = c.mass + (static_cast<size_t>(lb) * c.Hkv + kvh) * c.slots;
   for (int region = 0; region < 2; ++region) {
-    const int cnt_r = region ? n16 : n8;
     const int base = region ? c.cap8 : 0;
-    for (int j = tid; 4 * j < cnt_r; j += kThreads) {
-      float4 sv[8];
+    // tokens [lo, hi) of the region: all of them, or in a cluster this
+    // split's chunks only (lo is then a multiple of 16)
+    int lo = 0, hi = region ? n16 : n8;
+    if (ap.cluster) {
+      if (region == 0) {
+        lo = min(32 * cb, n8);
+        hi = min(32 * min(ce, nc8), n8);
+      } else {
+        lo = min(16 * max(cb - nc8, 0), n16);
+        hi = min(16 * max(ce - nc8, 0), n16);
+      }
+    }
+    const int jlo = lo >> 2, jhi = (hi + 3) >> 2;     // float4 groups of 4 tokens
+    // two float4 rows of every head per thread in flight; j runs from a
+    // multiple of 8 so that the 8 groups of a 128-byte line sit in one warp
+    for (int j0 = (jlo & ~7) + tid; j0 < jhi; j0 += 2 * kThreads) {
+      float4 sv[2][8];
 #pragma unroll
-      for (int h = 0; h < 8; ++h)
-        if (h < g)
-          sv[h] = __ldcg(reinterpret_cast<const float4*>(SC + static_cast<size_t>(h) * c.slots + base) + j);
-      float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int u = 0; u < 2; ++u) {
+        const int j = j0 + u * kThreads;
 #pragma unroll
-      for (int h = 0; h < 8; ++h)
-        if (h < g) {
-          a.x += ex2(fmaf(sv[h].x, kL2E, -ML[h])) * iL[h];
-          a.y += ex2(fmaf(sv[h].y, kL2E, -ML[h])) * iL[h];
-          a.z += ex2(fmaf(sv[h].z, kL2E, -ML[h])) * iL[h];
-          a.w += ex2(fmaf(sv[h].w, kL2E, -ML[h])) * iL[h];
-        }
-      // The raw scores are dead once read here (the next step rewrites every
-      // live slot before reading it): drop whole 128-byte lines of them from
-      // L2 so they are never written back.  The 8 lanes reading one line are
-      // in this warp; lines shared with a neighbouring row are kept.
-      __syncwarp(__activemask());
-      if ((j & 7) == 0 && 4 * j + 32 <= cnt_r) {
+        for (int h = 0; h < 8; ++h)
+          if (h < g && j >= jlo && j < jhi)
+            sv[u][h] = __ldcg(reinterpret_cast<const float4*>(SC + static_cast<size_t>(h) * c.slots + base) + j);
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int j = j0 + u * kThreads;
+        if (j < jlo || j >= jhi) continue;
+        float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
         for (int h = 0; h < 8; ++h)
           if (h < g) {
-            const float* line = SC + static_cast<size_t>(h) * c.slots + base + 4 * j;
-            if ((reinterpret_cast<uintptr_t>(line) & 127u) == 0) l2_discard_line(line);
+            a.x += ex2(fmaf(sv[u][h].x, kL2E, -ML[h])) * iL[h];
+            a.y += ex2(fmaf(sv[u][h].y, kL2E, -ML[h])) * iL[h];
+            a.z += ex2(fmaf(sv[u][h].z, kL2E, -ML[h])) * iL[h];
+            a.w += ex2(fmaf(sv[u][h].w, kL2E, -ML[h])) * iL[h];
           }
+        // The raw scores are dead once read here (the next step rewrites every
+        // live slot before reading it): drop whole 128-byte lines of them from
+        // L2 so they are never written back.  The 8 lanes reading one line are
+        // in this warp; lines shared with a neighbouring row are kept.
+        __syncwarp(__activemask());
+        if ((j & 7) == 0 && 4 * j + 32 <= hi) {
+#pragma unroll
+          for (int h = 0; h < 8; ++h)
+            if (h < g) {
+              const float* line = SC + static_cast<size_t>(h) * c.slots + base + 4 * j;
+              if ((reinterpret_cast<uintptr_t>(line) & 127u) == 0) l2_discard_line(line);
+            }
+        }
+        // slots past the region end hold stale scores; their mass is never read
+        reinterpret_cast<float4*>(MS + base)[j] = a;
       }
-      // slots past the region end hold stale scores; their mass is never read
-      reinterpret_cast<float4*>(MS + base)[j] = a;
     }
   }
 }
@@ -753,8 +891,40 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const cudaError_t e = launch_pdl(k_attn_mma<D, TMA>, dim3(ap.nlb * c.Hkv, ap.splits),
-                                   dim3(kThreads), smem, s, c, ap, tm);
+  AttnParams a = ap;
+  a.cluster = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ap.nlb * c.Hkv, ap.splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (ap.splits >= 2 && ap.splits <= kMaxClusterSplits) {
+    // the splits of a unit as one cluster, where the device can co-schedule it
+    static int ok[kMaxClusterSplits + 1] = {};      // 0 unknown, 1 yes, -1 no
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = 1;
+    at[1].val.clusterDim.y = ap.splits;
+    at[1].val.clusterDim.z = 1;
+    if (ok[ap.splits] == 0) {
+      cudaLaunchConfig_t q = cfg;
+      q.attrs = at + 1;
+      q.numAttrs = 1;
+      int n = 0;
+      const cudaError_t oe = cudaOccupancyMaxActiveClusters(&n, k_attn_mma<D, TMA>, &q);
+      ok[ap.splits] = (oe == cudaSuccess && n > 0) ? 1 : -1;
+      if (oe != cudaSuccess) (void)cudaGetLastError();
+    }
+    if (ok[ap.splits] == 1) {
+      a.cluster = 1;
+      cfg.numAttrs = 2;
+    }
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_mma<D, TMA>, c, a, tm);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

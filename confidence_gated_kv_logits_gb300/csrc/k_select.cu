@@ -192,11 +192,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_select(Cache c, StepParams sp) 
   const int l = lb / c.B, b = lb % c.B;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_trigger();     // the attention may be scheduled (it waits for this grid)
-  // n8, n16, positions, EMA and mass come from the previous step, which the
-  // confidence kernel has already waited for; the budget is read after
-  // pdl_wait() below
+  // n8, n16, the step count, positions, EMA and mass come from the previous
+  // step, which the confidence kernel has already waited for; the budget is
+  // read after pdl_wait() below
   const int n8 = c.n8[lb], n16 = c.n16[lb];
-  const int t = sp.t;
+  const int nstep = c.tstep[lb];
+  const int t = sp.t0 + nstep;
   const int Hkv = c.Hkv, cap8 = c.cap8, W = c.W, P = c.P, d = c.d;
   int32_t* pos8 = c.pos8 + static_cast<size_t>(lb) * cap8;
   int32_t* pos16 = c.pos16 + static_cast<size_t>(lb) * c.Wr;
@@ -574,7 +575,8 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
   {
     // FP16 moves and the new token: (move, KV head, 16-byte piece) items,
     // 4 loads in flight per thread
-    const int cpr = d / 8, per = 2 * cpr, items = (nmov16 + 1) * Hkv * per;
+    const int cpr = d / 8, per = 2 * cpr,
+              items = (nmov16 + (sp.defer_new ? 0 : 1)) * Hkv * per;
     for (int base = 0; base < items; base += 4 * kThreads) {
       int4 v[4];
       __half* dst[4];
@@ -612,6 +614,9 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
     const int hn = sj16[nmov16].x;
     pos16[hn] = t;
     ema16[hn] = 0.0f;
+    if (sp.defer_new) c.new_slot[lb] = hn;
+    c.tstep[lb] = nstep + 1;
+    if (lb == 0) c.stats->steps += 1ull;
   }
   __syncthreads();
 
@@ -644,6 +649,36 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
                   (static_cast<unsigned long long>(n8n) * (2ull * d + 8ull) +
                    static_cast<unsigned long long>(n16n) * 4ull * d));
   }
+}
+
+// The arriving token of a deferred selection, one CTA per (layer, sequence):
+// its K/V rows go to the FP16 slot the selection reserved, then the kept
+// positions (INT8 slots, then FP16 slots) are reported.
+__global__ void __launch_bounds__(kThreads) k_append(Cache c, StepParams sp) {
+  const int lb = sp.lb0 + blockIdx.x;
+  const int lbu = blockIdx.x;                 // index into the caller's buffers
+  const int tid = threadIdx.x;
+  pdl_trigger();     // the attention reads only its queries before its own wait
+  pdl_wait();        // the selection that reserved the slot is complete
+  const int Hkv = c.Hkv, d = c.d, hn = c.new_slot[lb];
+  const int cpr = d / 8, items = Hkv * 2 * cpr;    // 16-byte pieces of K and V
+  for (int it = tid; it < items; it += kThreads) {
+    const int h = it / (2 * cpr), pc = it - h * 2 * cpr;
+    const bool isv = pc >= cpr;
+    const int ch = isv ? pc - cpr : pc;
+    const size_t u = static_cast<size_t>(lb) * Hkv + h;
+    const int4 v = reinterpret_cast<const int4*>((isv ? sp.v_new : sp.k_new) +
+                                                 (static_cast<size_t>(lbu) * Hkv + h) * d)[ch];
+    reinterpret_cast<int4*>((isv ? c.v16 : c.k16) + (u * c.Wr + hn) * d)[ch] = v;
+  }
+  const int n8 = c.n8[lb], n16 = c.n16[lb];
+  if (sp.kept_pos) {
+    const int32_t* pos8 = c.pos8 + static_cast<size_t>(lb) * c.cap8;
+    const int32_t* pos16 = c.pos16 + static_cast<size_t>(lb) * c.Wr;
+    int32_t* __restrict__ kp = sp.kept_pos + static_cast<size_t>(lbu) * c.Ncap;
+    for (int i = tid; i < n8 + n16; i += kThreads) kp[i] = (i < n8) ? pos8[i] : pos16[i - n8];
+  }
+  if (sp.kept_count && tid == 0) sp.kept_count[lbu] = n8 + n16;
 }
 
 }  // namespace
@@ -682,6 +717,11 @@ cudaError_t launch_select(const Cache& c, const StepParams& sp, cudaStream_t s) 
     case CONFKV_POLICY_RANDOM: return launch_select_p<CONFKV_POLICY_RANDOM>(c, sp, smem, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_append(const Cache& c, const StepParams& sp, cudaStream_t s) {
+  const cudaError_t e = launch_pdl(k_append, dim3(sp.nlb), dim3(kThreads), 0, s, c, sp);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace confkv

@@ -35,12 +35,16 @@
  *     (non-finite logits, a wait that timed out) are latched in device memory
  *     and returned by the next confkv_stats() call.  No exception crosses the
  *     ABI; no call traps the GPU.
- *   - confkv_step never synchronises the host with the GPU and allocates
- *     nothing, so steps can be captured in a CUDA graph once the context
- *     exists.  The step's position is a launch parameter taken from the
- *     host-side counter, which advances at capture time: a captured graph
- *     replays exactly the steps it recorded, once, and must not be replayed
- *     again (capture anew for the next steps).
+ *   - confkv_step, confkv_step_begin and confkv_step_layer never synchronise
+ *     the host with the GPU and allocate nothing, so a decode step (one
+ *     confkv_step, or a confkv_step_begin followed by every layer's
+ *     confkv_step_layer) can be captured in a CUDA graph once the context has
+ *     been prefilled.  All step state, the position included, lives in device
+ *     memory: each replay of the graph is one further decode step that reads
+ *     the buffers captured (the caller writes the next step's inputs into
+ *     them before the replay), and replays mix freely with eager steps.
+ *     Only the host-side argument checks (the per-layer order, the position
+ *     overflow check) see the capture and not the replays.
  */
 #ifndef CONFKV_H_
 #define CONFKV_H_
@@ -115,8 +119,9 @@ typedef struct confkv_opts {
 
 /* Counters read back by confkv_stats (cumulative since create unless noted). */
 typedef struct confkv_stats_t {
-  int64_t steps;            /* decode steps run */
-  int64_t position;         /* position of the next token */
+  int64_t steps;            /* decode steps run, graph replays included (a
+                               per-layer step counts from confkv_step_begin) */
+  int64_t position;         /* position of the next arriving token */
   int32_t error_flags;      /* CONFKV_FLAG_* bits latched since the last call */
   int32_t reserved;
   int64_t tokens_evicted;   /* over all (layer, sequence) */
@@ -199,20 +204,25 @@ int confkv_step(confkv_ctx* ctx, const float* logits, const uint16_t* q,
  * time (the layers of a decode step are not all known up front):
  *
  * confkv_step_begin -- first stage of a decode step: the confidence and the
- * budget of every sequence from this step's logits (as in confkv_step).
+ * budget of every sequence from this step's logits (as in confkv_step), then
+ * the EMA update, ranking, eviction, compaction and INT8 aging of every
+ * layer's caches in one launch (none of it depends on the new token's K/V),
+ * reserving each layer's FP16 slot for its arriving token.
  *   logits fp32 [B][V]; conf_out fp32 [B] and budget_out int32 [B] may be NULL.
  * CONFKV_ERR_STATE if the previous begun step still has layers to run.
  *
- * confkv_step_layer -- the rest of the step for one layer `layer`: EMA update,
- * ranking, eviction, compaction + INT8 aging and attention of that layer's B
- * caches.  Buffers hold that layer only:
+ * confkv_step_layer -- the rest of the step for one layer `layer`: the
+ * arriving token's K/V rows go to the reserved slots, then the attention of
+ * that layer's B caches.  Buffers hold that layer only:
  *   q fp16 [B][Hq][d]; k_new, v_new fp16 [B][Hkv][d] (all three 16-byte aligned);
  *   out fp32 [B][Hq][d]; kept_pos int32 [B][N_max] and kept_count int32 [B]
  *   may be NULL.
  * Every layer must be run exactly once, in any order; the step (and the
- * position) advances after the last one.  CONFKV_ERR_STATE without a begun
- * step or for a layer already run; CONFKV_ERR_INVALID_ARG for a bad layer.
- * The results equal confkv_step's for the same inputs.
+ * position) advances after the last one.  Until a layer has run, its caches
+ * hold the step's compacted state without the arriving token's K/V rows.
+ * CONFKV_ERR_STATE without a begun step or for a layer already run;
+ * CONFKV_ERR_INVALID_ARG for a bad layer.  The results equal confkv_step's
+ * for the same inputs.
  */
 int confkv_step_begin(confkv_ctx* ctx, const float* logits, float* conf_out,
                       int32_t* budget_out, void* stream);
@@ -255,8 +265,9 @@ int confkv_read_cache(confkv_ctx* ctx, int l, int b, int cap, int* n8, int* n16,
                       float* vs, uint16_t* k16, uint16_t* v16, float* mass);
 
 /*
- * Per-kernel CUDA-event timing of the step kernels (0 confidence, 1 select,
- * 2 compact, 3 attention).  confkv_profile_enable(ctx, mask) synchronises,
+ * Per-kernel CUDA-event timing of the step kernels (0 confidence, 1 select:
+ * EMA, ranking, eviction, compaction and INT8 aging, 2 append: the arriving
+ * token of one layer under per-layer stepping, 3 attention).  confkv_profile_enable(ctx, mask) synchronises,
  * clears the totals and records an event pair around every launch of each
  * kernel whose bit is set in `mask` (0 disables).  confkv_profile_read
  * synchronises and returns launches and total milliseconds per kernel.

@@ -26,12 +26,15 @@ def _T(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
-@pytest.mark.parametrize("d,splits", [(128, 1), (128, 3), (64, 2)])
-def test_per_layer_equals_full_step_bitwise(d, splits):
+@pytest.mark.parametrize("d,splits,kernel", [(128, 1, 0), (128, 3, 0), (64, 2, 0), (128, 5, 0),
+                                             (128, 2, 1), (64, 1, 1)])
+def test_per_layer_equals_full_step_bitwise(d, splits, kernel):
+    # kernel 0: the tensor-core attention stores the arriving token itself;
+    # kernel 1: the CUDA-core attention after a separate append launch
     import confidence_gated_kv_logits_gb300 as pkg
     w = small(d=d)
-    a = pkg.ConfKV.for_workload(w, device=0, attn_splits=splits)
-    b = pkg.ConfKV.for_workload(w, device=0, attn_splits=splits)
+    a = pkg.ConfKV.for_workload(w, device=0, attn_splits=splits, attn_kernel=kernel)
+    b = pkg.ConfKV.for_workload(w, device=0, attn_splits=splits, attn_kernel=kernel)
     kvs = [[wl.prefill_kv_lb(w, l, bb) for bb in range(w.B)] for l in range(w.L)]
     K = np.stack([np.stack([x[0] for x in row]) for row in kvs])
     V = np.stack([np.stack([x[1] for x in row]) for row in kvs])
@@ -99,37 +102,77 @@ def test_per_layer_state_errors():
     kv.close()
 
 
-def test_step_captured_in_cuda_graph_equals_eager():
-    # a step captured in a CUDA graph (allocation-free, no host sync) and
-    # replayed once gives the same bits as the same step run eagerly
+def _eager_and_graph(w, per_layer, n_eager, n_replay):
+    """Runs n_eager eager steps, then n_replay more either eagerly or as
+    replays of one captured step; returns the last outputs of each run."""
     import confidence_gated_kv_logits_gb300 as pkg
-    w = small(L=2, B=2, steps=12)
-    outs = []
+    results = []
     for graph in (False, True):
         kv = pkg.ConfKV.for_workload(w, device=0)
+        kvs = [[wl.prefill_kv_lb(w, l, bb) for bb in range(w.B)] for l in range(w.L)]
+        K = np.stack([np.stack([x[0] for x in row]) for row in kvs])
+        V = np.stack([np.stack([x[1] for x in row]) for row in kvs])
+        kv.prefill(_T(K), _T(V), w.prefill)
+        # the buffers a captured step reads and writes
+        lg = torch.zeros(w.B, w.V, device=DEV)
+        q = torch.zeros(w.L, w.B, w.Hq, w.d, dtype=torch.float16, device=DEV)
+        k = torch.zeros(w.L, w.B, w.Hkv, w.d, dtype=torch.float16, device=DEV)
+        v = torch.zeros_like(k)
         out = torch.zeros(w.L, w.B, w.Hq, w.d, device=DEV)
         kp = torch.full((w.L, w.B, kv.Ncap), -1, dtype=torch.int32, device=DEV)
         kc = torch.zeros(w.L, w.B, dtype=torch.int32, device=DEV)
-        inputs = [tuple(torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
-                        for x in wl.step_inputs(w, s)) for s in range(w.steps)]
-        torch.cuda.synchronize()
-        for s in range(w.steps - 1):
-            kv.step(*inputs[s], out, kp, kc)
-        last = inputs[-1]
-        if graph:
-            stream = torch.cuda.Stream()
-            stream.wait_stream(torch.cuda.current_stream())
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                kv.step(*last, out, kp, kc, stream=stream)
-            g.replay()
-        else:
-            kv.step(*last, out, kp, kc)
+        conf = torch.zeros(w.B, device=DEV)
+        bud = torch.zeros(w.B, dtype=torch.int32, device=DEV)
+
+        def load(s):
+            for dst, src in zip((lg, q, k, v), wl.step_inputs(w, s)):
+                dst.copy_(torch.from_numpy(np.ascontiguousarray(src)))
+
+        def one_step(stream=None):
+            if not per_layer:
+                kv.step(lg, q, k, v, out, kp, kc, conf, bud, stream=stream)
+                return
+            kv.step_begin(lg, conf, bud, stream=stream)
+            for l in range(w.L):
+                kv.step_layer(l, q[l], k[l], v[l], out[l], kp[l], kc[l], stream=stream)
+
+        for s in range(n_eager):
+            load(s)
+            one_step()
+        g = None
+        for s in range(n_eager, n_eager + n_replay):
+            load(s)
+            if not graph:
+                one_step()
+            elif g is None:
+                # capturing enqueues nothing: the first replay is this step
+                torch.cuda.synchronize()
+                stream = torch.cuda.Stream()
+                stream.wait_stream(torch.cuda.current_stream())
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    one_step(stream)
+                g.replay()
+            else:
+                g.replay()
         torch.cuda.synchronize()
         st, rc = kv.stats()
-        assert rc == 0 and st["steps"] == w.steps
-        outs.append((out.cpu().numpy(), kp.cpu().numpy(), kc.cpu().numpy()))
+        assert rc == 0
+        assert st["steps"] == n_eager + n_replay
+        assert st["position"] == w.prefill + n_eager + n_replay
+        results.append([x.cpu().numpy() for x in (out, kp, kc, conf, bud)])
         kv.close()
-    for a, b in zip(outs[0], outs[1]):
-        assert np.array_equal(a.view(np.uint32) if a.dtype == np.float32 else a,
-                              b.view(np.uint32) if b.dtype == np.float32 else b)
+    return results
+
+
+@pytest.mark.parametrize("per_layer", [False, True])
+def test_step_graph_replayed_equals_eager(per_layer):
+    # one captured step replayed for several decode steps (new inputs written
+    # into the captured buffers before each replay) gives the same bits as
+    # the same steps run eagerly: the position and all state are on the device
+    w = small(L=3, B=2, steps=20)
+    eager, graph = _eager_and_graph(w, per_layer, n_eager=4, n_replay=14)
+    for a, b in zip(eager, graph):
+        if a.dtype == np.float32:
+            a, b = a.view(np.uint32), b.view(np.uint32)
+        assert np.array_equal(a, b)

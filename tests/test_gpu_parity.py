@@ -132,7 +132,8 @@ def test_gqa8_d64_pyramid():
     _check(parity.run(w))
 
 
-@pytest.mark.parametrize("splits", [1, 3])
+# 2..8 splits merge inside a thread-block cluster, 12 through global memory
+@pytest.mark.parametrize("splits", [1, 3, 8, 12])
 @pytest.mark.parametrize("kernel,tma", [(1, 0), (2, 0), (2, -1)])
 def test_forced_split_counts_and_kernels(splits, kernel, tma):
     w = small(prefill=90, steps=40, V=64)
