@@ -23,6 +23,9 @@ using confkv::StepParams;
 namespace {
 
 constexpr int kSmCount = 152;
+// resident tensor-core attention CTAs per SM (register-bound): 3 at head_dim
+// 128, 4 at head_dim 64
+int attn_ctas_per_sm(int d) { return d == 64 ? 4 : 3; }
 constexpr int kProfKernels = 4;
 // "select" covers ranking, eviction, compaction moves and INT8 aging; slot 2
 // is unused (kept so that the kernel mask bits stay stable).
@@ -149,18 +152,35 @@ void prof_collect(confkv_ctx* c) {
 // WINDOW keeps a fixed budget (N_low) and computes no confidence
 bool uses_confidence(const confkv_ctx* c) { return c->policy != CONFKV_POLICY_WINDOW; }
 
-int auto_splits(int units, int ncap) {
-  const int want = (4 * kSmCount + units - 1) / units;
-  const int tok_lim = std::max(1, (ncap + 1 + 127) / 128);
-  return std::max(1, std::min(std::min(want, tok_lim), 16));
+// Largest power of two <= x (x >= 1): odd split counts measured slower (their
+// clusters and chunk shares are uneven).
+int floor_pow2(int x) {
+  int p = 1;
+  while (2 * p <= x) p *= 2;
+  return p;
+}
+
+// Split-K count of a whole-step attention launch: as many splits as still
+// fit every CTA in one wave (3 or 4 resident CTAs per SM), at least ~512
+// cached tokens per split (by the budget), at most one cluster (8), a power
+// of two.
+// Measured on GB300: a second wave, or splits of a few chunks per warp, cost
+// more than the idle SMs they would fill (Qwen-14B shape, 384 units: 1 split
+// 48 us, 2 splits 60 us; gpt-oss shape, 192 units: 2 splits 31 us, 3 splits
+// 43 us, 4 splits 39 us).
+int auto_splits(int units, int ncap, int d) {
+  const int want = std::max(1, attn_ctas_per_sm(d) * kSmCount / units);
+  const int tok_lim = std::max(1, (ncap + 1) / 512);
+  return floor_pow2(std::max(1, std::min(std::min(want, tok_lim), 8)));
 }
 
 // One layer's launch holds few units, so its time is one CTA's latency: about
-// two CTAs per SM in a single wave, at most one cluster (8 splits) per unit.
+// two CTAs per SM, same token floor, cap and rounding (Qwen-32B shape, 64
+// units per layer: 4 splits 14.4 us per layer, 8 splits 21.6 us).
 int auto_splits_layer(int units, int ncap) {
   const int want = std::max(1, 2 * kSmCount / units);
-  const int tok_lim = std::max(1, (ncap + 1 + 127) / 128);
-  return std::max(1, std::min(std::min(want, tok_lim), 8));
+  const int tok_lim = std::max(1, (ncap + 1) / 512);
+  return floor_pow2(std::max(1, std::min(std::min(want, tok_lim), 8)));
 }
 
 int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s, int lb0, int nlb,
@@ -252,7 +272,7 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   if (o.attn_splits > 0) {
     c->splits = c->splits_layer = o.attn_splits;
   } else {
-    c->splits = auto_splits(units, c->Ncap);
+    c->splits = auto_splits(units, c->Ncap, c->d);
     c->splits_layer = auto_splits_layer(c->B * c->Hkv, c->Ncap);
   }
   const int max_splits = std::max(c->splits, c->splits_layer);

@@ -287,8 +287,14 @@ struct SoftState {
   int E;                  // O holds values scaled by 2^E
 };
 
+// Resident CTAs per SM: 3 at head_dim 128 (registers and the 74 KB of TMA
+// stages); 4 at head_dim 64 (<= 128 registers, 35 KB of stages), whose
+// half-size chunks need the extra warps to keep the loads in flight.
 template <int D, bool TMA>
-__global__ void __launch_bounds__(kThreads, 3)
+constexpr int kCtasPerSm = (D == 64 && !TMA) ? 4 : 3;
+
+template <int D, bool TMA>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm<D, TMA>)
 k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   using G = Geo<D>;
   static_assert(!TMA || D == 128, "the TMA path is specialised for head_dim 128");
