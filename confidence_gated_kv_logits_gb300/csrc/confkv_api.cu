@@ -320,7 +320,7 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
     e = cudaMemcpy(c->btab, bt.data(), bt.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
-  if (e == cudaSuccess && c->d == 128 && o.attn_tma >= 0) c->has_tmaps = confkv::encode_attention_maps(c->cache, c->tmaps);
+  if (e == cudaSuccess && o.attn_tma >= 0) c->has_tmaps = confkv::encode_attention_maps(c->cache, c->tmaps);
   if (e != cudaSuccess) {
     const bool oom = (e == cudaErrorMemoryAllocation);
     cudaGetLastError();

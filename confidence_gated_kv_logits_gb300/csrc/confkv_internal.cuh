@@ -163,7 +163,7 @@ cudaError_t launch_attention(const Cache& c, const AttnParams& ap, cudaStream_t 
 // AttnParams::kernel (only that kernel handles AttnParams::k_new)
 bool attention_uses_mma(const Cache& c, int kernel);
 cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStream_t s);
-// Encodes the four tensor maps of the d = 128 TMA attention path into `out`
+// Encodes the four tensor maps of the TMA attention path into `out`
 // (kTmaMapsBytes bytes, 64-byte aligned); returns false if the driver cannot
 // or the cache is too large for 32-bit tile coordinates.
 constexpr int kTmaMapsBytes = 512;

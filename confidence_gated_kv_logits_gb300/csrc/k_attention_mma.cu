@@ -149,7 +149,14 @@ __device__ __forceinline__ float pow2i(int e) {
 }
 
 // ---- TMA (tensor-map tile loads, 128-byte swizzle) + mbarrier helpers ----
-constexpr int kTmaStage = 9216;                  // K tile 4 KB | V tile 4 KB | scales | pad
+// TMA stage of one warp: INT8 chunk = K tile (32 rows) | V tile | 2 x 32 scales,
+// FP16 chunk = K tile (16 rows) | V tile; every tile 1024-byte aligned
+// (swizzle atoms).  d = 128: 4 KB tiles, 9216 B stages; d = 64: 2 KB tiles,
+// 5120 B stages.
+template <int D>
+constexpr int kTmaTile = 32 * D;
+template <int D>
+constexpr int kTmaStage = (D == 128) ? 9216 : 5120;
 constexpr unsigned kWaitSpins = 1u << 26;        // bounded mbarrier wait (then flag + bail)
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
@@ -200,31 +207,43 @@ __device__ __forceinline__ void bulk_1d(uint32_t dst, const void* src, unsigned 
 __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int ch) {
   return tile + static_cast<uint32_t>(row * 128 + ((ch ^ (row & 7)) << 4));
 }
+// address of 16-byte chunk `ch` (0..3) of row `row` in a 64-byte-swizzled tile
+// of 64-byte rows (the 16-byte chunk index is XORed with address bits 7..8)
+__device__ __forceinline__ uint32_t swz64(uint32_t tile, int row, int ch) {
+  return tile + static_cast<uint32_t>(row * 64 + ((ch ^ ((row >> 1) & 3)) << 4));
+}
 
 struct TmaMaps {
   CUtensorMap k8, v8, k16, v16;
 };
 
-// TMA issue of one chunk (d = 128) by one lane: INT8 chunk = K and V tiles of
-// 32 rows x 128 B + the 2 x 32 scales; FP16 chunk = K and V tiles of 16 rows
-// x 256 B as two 128-byte-wide boxes each.
+// TMA issue of one chunk by one lane.  INT8 chunk: K and V tiles of 32 rows x
+// D bytes + the 2 x 32 scales.  FP16 chunk: K and V tiles of 16 rows x 2D
+// bytes, as 128-byte-wide boxes (two per row at d = 128, one at d = 64).
+template <int D>
 __device__ __forceinline__ void issue_chunk_tma(const Cache& c, const TmaMaps& tm, int unit,
                                                 int nc8, int ci, uint32_t st, uint32_t bar) {
+  constexpr int T = kTmaTile<D>;
   const uint64_t pol = evict_first_policy();
   if (ci < nc8) {
     const int row0 = unit * c.cap8 + 32 * ci;
-    mbar_expect_tx(bar, 2 * 4096 + 256);
+    mbar_expect_tx(bar, 2 * T + 256);
     tma_2d(st, &tm.k8, 0, row0, bar, pol);
-    tma_2d(st + 4096, &tm.v8, 0, row0, bar, pol);
-    bulk_1d(st + 8192, c.ks + row0, 128, bar);
-    bulk_1d(st + 8192 + 128, c.vs + row0, 128, bar);
+    tma_2d(st + T, &tm.v8, 0, row0, bar, pol);
+    bulk_1d(st + 2 * T, c.ks + row0, 128, bar);
+    bulk_1d(st + 2 * T + 128, c.vs + row0, 128, bar);
   } else {
     const int row0 = unit * c.Wr + 16 * (ci - nc8);
-    mbar_expect_tx(bar, 2 * 4096);
-    tma_2d(st, &tm.k16, 0, row0, bar, pol);
-    tma_2d(st + 2048, &tm.k16, 64, row0, bar, pol);
-    tma_2d(st + 4096, &tm.v16, 0, row0, bar, pol);
-    tma_2d(st + 6144, &tm.v16, 64, row0, bar, pol);
+    mbar_expect_tx(bar, 2 * T);
+    if constexpr (D == 128) {
+      tma_2d(st, &tm.k16, 0, row0, bar, pol);
+      tma_2d(st + 2048, &tm.k16, 64, row0, bar, pol);
+      tma_2d(st + 4096, &tm.v16, 0, row0, bar, pol);
+      tma_2d(st + 6144, &tm.v16, 64, row0, bar, pol);
+    } else {
+      tma_2d(st, &tm.k16, 0, row0, bar, pol);
+      tma_2d(st + 2048, &tm.v16, 0, row0, bar, pol);
+    }
   }
 }
 
@@ -288,17 +307,16 @@ struct SoftState {
 };
 
 // Resident CTAs per SM: 3 at head_dim 128 (registers and the 74 KB of TMA
-// stages); 4 at head_dim 64 (<= 128 registers, 35 KB of stages), whose
+// stages); 4 at head_dim 64 (<= 128 registers, 35-41 KB of stages), whose
 // half-size chunks need the extra warps to keep the loads in flight.
 template <int D, bool TMA>
-constexpr int kCtasPerSm = (D == 64 && !TMA) ? 4 : 3;
+constexpr int kCtasPerSm = (D == 64) ? 4 : 3;
 
 template <int D, bool TMA>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm<D, TMA>)
 k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   using G = Geo<D>;
-  static_assert(!TMA || D == 128, "the TMA path is specialised for head_dim 128");
-  constexpr int STAGE = TMA ? kTmaStage : G::STAGE;
+  constexpr int STAGE = TMA ? kTmaStage<D> : G::STAGE;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // TMA path: 1024-byte aligned base for the 128-byte swizzle atoms (its
   // launch allocates 1024 bytes of slack for this); the cp.async path needs
@@ -460,7 +478,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     if constexpr (TMA) {
       if (lane == 0 && i < cnt) {
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        issue_chunk_tma(c, tm, unit, nc8, cb + warp + kWarps * i, wbase + (i % kStages) * STAGE,
+        issue_chunk_tma<D>(c, tm, unit, nc8, cb + warp + kWarps * i, wbase + (i % kStages) * STAGE,
                         smem_u32(&bars[warp][i % kStages]));
       }
     } else {
@@ -486,7 +504,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     const uint32_t st = wbase + (i % kStages) * STAGE;
     if (ci < nc8) {
       // ------------------------- INT8 chunk: 32 tokens -------------------------
-      const uint32_t sks = st + (TMA ? 8192 : G::DATA), svs = sks + 128;
+      const uint32_t sks = st + (TMA ? 2 * kTmaTile<D> : G::DATA), svs = sks + 128;
       const int tb = 32 * ci;
       uint32_t kw[2][2][G::KS];
 #pragma unroll
@@ -495,8 +513,10 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
         for (int r = 0; r < 2; ++r)
 #pragma unroll
           for (int u = 0; u < G::KPT / 16; ++u) {
-            const uint4 v = TMA ? lds128(swz(st, 16 * sb + gid + 8 * r, 2 * t4 + u))
-                                : lds128(tp(st, lane, (2 * sb + r) * G::KPT + 16 * u));
+            const int row = 16 * sb + gid + 8 * r;
+            const uint4 v = !TMA    ? lds128(tp(st, lane, (2 * sb + r) * G::KPT + 16 * u))
+                            : D == 128 ? lds128(swz(st, row, 2 * t4 + u))
+                                       : lds128(swz64(st, row, t4));
             kw[sb][r][4 * u] = v.x;
             kw[sb][r][4 * u + 1] = v.y;
             kw[sb][r][4 * u + 2] = v.z;
@@ -568,7 +588,9 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
             vw[ii][2] = v.z;
             vw[ii][3] = v.w;
           } else {
-            const uint2 v = lds64(tp(st, lane, b));
+            const int row = 16 * sb + 2 * t4 + (ii & 1) + 8 * (ii >> 1);
+            const uint2 v = TMA ? lds64(swz64(st + kTmaTile<D>, row, gid >> 1) + 8 * (gid & 1))
+                                : lds64(tp(st, lane, b));
             vw[ii][0] = v.x;
             vw[ii][1] = v.y;
           }
@@ -584,8 +606,9 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       for (int r = 0; r < 2; ++r)
 #pragma unroll
         for (int u = 0; u < G::KPT / 8; ++u) {
-          const uint4 v = TMA ? lds128(swz(st + 2048 * (t4 >> 1), gid + 8 * r, 4 * (t4 & 1) + u))
-                              : lds128(tp(st, lane, r * G::KPT * 2 + 16 * u));
+          const uint4 v = !TMA    ? lds128(tp(st, lane, r * G::KPT * 2 + 16 * u))
+                          : D == 128 ? lds128(swz(st + 2048 * (t4 >> 1), gid + 8 * r, 4 * (t4 & 1) + u))
+                                     : lds128(swz(st, gid + 8 * r, 2 * t4 + u));
           kw[r][4 * u] = v.x;
           kw[r][4 * u + 1] = v.y;
           kw[r][4 * u + 2] = v.z;
@@ -631,8 +654,9 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
 #pragma unroll
         for (int u = 0; u < G::VPT / 8; ++u) {
           const int row = 2 * t4 + (ii & 1) + 8 * (ii >> 1);
-          const uint4 v = TMA ? lds128(swz(st + 4096 + 2048 * (gid >> 2), row, 2 * (gid & 3) + u))
-                              : lds128(tp(st, lane, D + ii * G::VPT * 2 + 16 * u));
+          const uint4 v = !TMA    ? lds128(tp(st, lane, D + ii * G::VPT * 2 + 16 * u))
+                          : D == 128 ? lds128(swz(st + 4096 + 2048 * (gid >> 2), row, 2 * (gid & 3) + u))
+                                     : lds128(swz(st + 2048, row, gid));
           vw[ii][4 * u] = v.x;
           vw[ii][4 * u + 1] = v.y;
           vw[ii][4 * u + 2] = v.z;
@@ -889,7 +913,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
 
 template <int D, bool TMA>
 cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm, cudaStream_t s) {
-  const int smem = kWarps * kStages * (TMA ? kTmaStage : Geo<D>::STAGE) + (TMA ? 1024 : 0);
+  const int smem = kWarps * kStages * (TMA ? kTmaStage<D> : Geo<D>::STAGE) + (TMA ? 1024 : 0);
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e = cudaFuncSetAttribute(k_attn_mma<D, TMA>,
@@ -937,7 +961,7 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
 }  // namespace
 
 bool encode_attention_maps(const Cache& c, void* out) {
-  if (c.d != 128) return false;
+  if (c.d != 128 && c.d != 64) return false;
   {
     // tile coordinates are signed 32-bit
     const unsigned long long u = static_cast<unsigned long long>(c.L) * c.B * c.Hkv;
@@ -958,22 +982,27 @@ bool encode_attention_maps(const Cache& c, void* out) {
   std::memset(&tm, 0, sizeof(tm));
   const cuuint64_t units = static_cast<cuuint64_t>(c.L) * c.B * c.Hkv;
   const cuuint32_t estr[2] = {1, 1};
+  const cuuint64_t D = static_cast<cuuint64_t>(c.d);
   {
-    const cuuint64_t dims[2] = {128, units * c.cap8};
-    const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {128, 32};
+    // INT8 rows of d bytes, 32-row boxes; d = 128: 128-byte swizzle, d = 64:
+    // 64-byte swizzle
+    const cuuint64_t dims[2] = {D, units * c.cap8};
+    const cuuint64_t strides[1] = {D};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(D), 32};
+    const CUtensorMapSwizzle sw = (c.d == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if (enc(&tm.k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.k8, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
     if (enc(&tm.v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.v8, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
   }
   {
-    const cuuint64_t dims[2] = {128, units * c.Wr};
-    const cuuint64_t strides[1] = {256};
+    // FP16 rows of 2d bytes as 64-element (128-byte) boxes of 16 rows
+    const cuuint64_t dims[2] = {D, units * c.Wr};
+    const cuuint64_t strides[1] = {2 * D};
     const cuuint32_t box[2] = {64, 16};
     if (enc(&tm.k16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c.k16, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -993,6 +1022,10 @@ cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStrea
   if (c.g < 1 || c.g > 8) return cudaErrorInvalidValue;
   TmaMaps tm;
   if (c.d == 64) {
+    if (ap.tmaps) {
+      std::memcpy(&tm, ap.tmaps, sizeof(tm));
+      return launch_mma_d<64, true>(c, ap, tm, s);
+    }
     std::memset(&tm, 0, sizeof(tm));
     return launch_mma_d<64, false>(c, ap, tm, s);
   }

@@ -110,8 +110,8 @@ typedef struct confkv_opts {
   int attn_splits;   /* split-K factor of the attention (0 = automatic) */
   int attn_kernel;   /* 0 automatic (tensor cores when Hq/Hkv <= 8), 1 CUDA
                         cores, 2 tensor cores (requires Hq/Hkv <= 8) */
-  int attn_tma;      /* tensor-core attention at head_dim 128 stages K/V tiles
-                        with TMA (0, default) or with cp.async (-1) */
+  int attn_tma;      /* tensor-core attention stages K/V tiles with TMA
+                        (0, default) or with cp.async (-1) */
   int policy;        /* CONFKV_POLICY_* (default CONFKV) */
   int reserved;      /* must be 0 */
   uint64_t seed;     /* RANDOM policy: seed of the draws */

@@ -132,11 +132,14 @@ def test_gqa8_d64_pyramid():
     _check(parity.run(w))
 
 
-# 2..8 splits merge inside a thread-block cluster, 12 through global memory
+# 2..8 splits merge inside a thread-block cluster, 12 through global memory;
+# tma 0: TMA tiles (128-byte swizzle at d = 128, 64-byte INT8 swizzle at
+# d = 64), -1: cp.async staging
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("splits", [1, 3, 8, 12])
 @pytest.mark.parametrize("kernel,tma", [(1, 0), (2, 0), (2, -1)])
-def test_forced_split_counts_and_kernels(splits, kernel, tma):
-    w = small(prefill=90, steps=40, V=64)
+def test_forced_split_counts_and_kernels(splits, kernel, tma, d):
+    w = small(prefill=90, steps=40, V=64, d=d)
     _check(parity.run(w, splits=splits, kernel=kernel, tma=tma))
 
 
