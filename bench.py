@@ -396,6 +396,7 @@ def run_ours(args):
 
     # ---- device-timed run ----
     kv = pkg.ConfKV.for_workload(w)
+    attn_path = kv.attention_path()
     if w.prefill:
         Kp, Vp = sd.prefill_kv(w)
         ql = wl.q_last(w)
@@ -527,7 +528,7 @@ def run_ours(args):
             "config": workload_config(w, {"parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
                                           "decode_steps": S}),
             "roofline": {"bound": "hbm",
-                         "kernel": "attention (k_attn_mma, %s)" % ("TMA" if w.d == 128 else "cp.async"),
+                         "kernel": "attention (%s)" % attn_path,
                          "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_kind": f"{peak_kind} HBM copy",
                          "traffic": attention_traffic(),

@@ -33,7 +33,8 @@ FLAG_TIMEOUT = 4
 EXPORTS = ("confkv_create", "confkv_prefill", "confkv_step", "confkv_step_host",
            "confkv_stats", "confkv_read_cache", "confkv_profile_enable",
            "confkv_profile_read", "confkv_last_error", "confkv_free",
-           "confkv_confidence_noalloc", "confkv_step_begin", "confkv_step_layer")
+           "confkv_confidence_noalloc", "confkv_step_begin", "confkv_step_layer",
+           "confkv_attention_path")
 
 
 class ConfKVError(RuntimeError):
@@ -105,6 +106,8 @@ def load_library(path=LIB_PATH):
     L.confkv_last_error.argtypes = [vp]
     L.confkv_free.restype = None
     L.confkv_free.argtypes = [vp]
+    L.confkv_attention_path.restype = ci
+    L.confkv_attention_path.argtypes = [vp]
     L.confkv_confidence_noalloc.restype = ci
     L.confkv_confidence_noalloc.argtypes = [vp, ci, ci, cf, ci, ci, vp, vp, vp, vp]
     _lib = L
@@ -241,6 +244,15 @@ class ConfKV:
                 _hptr(conf, np.float32, B, "conf"),
                 _hptr(budget, np.int32, B, "budget")]
         self._check(self._L.confkv_step_host(self._h, *args, self._stream(stream)))
+
+    ATTN_PATHS = ("cuda-core", "tensor-core cp.async", "tensor-core TMA")
+
+    def attention_path(self):
+        """Name of the attention kernel this context runs."""
+        r = self._L.confkv_attention_path(self._h)
+        if r < 0:
+            self._check(r)
+        return self.ATTN_PATHS[r]
 
     def stats(self, check=True):
         s = Stats()

@@ -690,6 +690,12 @@ int confkv_profile_read(confkv_ctx* c, confkv_profile_t* out) {
   return CONFKV_OK;
 }
 
+int confkv_attention_path(const confkv_ctx* c) {
+  if (!c) return CONFKV_ERR_INVALID_ARG;
+  if (!confkv::attention_uses_mma(c->cache, c->attn_kernel)) return CONFKV_ATTN_CUDA_CORE;
+  return c->has_tmaps ? CONFKV_ATTN_TENSOR_TMA : CONFKV_ATTN_TENSOR_CP_ASYNC;
+}
+
 const char* confkv_last_error(const confkv_ctx* c) { return c ? c->msg.c_str() : "null context"; }
 
 void confkv_free(confkv_ctx* c) {

@@ -305,6 +305,17 @@ int confkv_confidence_noalloc(const float* logits, int batch, int vocab, float t
                               int N_low, int N_high, float* conf_out, int32_t* budget_out,
                               int32_t* flags_out, void* stream);
 
+/*
+ * Which attention kernel the context's steps run (fixed at create):
+ * CONFKV_ATTN_CUDA_CORE (Hq/Hkv > 8 or forced), CONFKV_ATTN_TENSOR_CP_ASYNC
+ * (tensor cores, K/V tiles staged with cp.async), CONFKV_ATTN_TENSOR_TMA
+ * (tensor cores, K/V tiles by TMA); CONFKV_ERR_INVALID_ARG for NULL.
+ */
+#define CONFKV_ATTN_CUDA_CORE 0
+#define CONFKV_ATTN_TENSOR_CP_ASYNC 1
+#define CONFKV_ATTN_TENSOR_TMA 2
+int confkv_attention_path(const confkv_ctx* ctx);
+
 /* Message of the last error of this context (never NULL). */
 const char* confkv_last_error(const confkv_ctx* ctx);
 

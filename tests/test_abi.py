@@ -71,6 +71,7 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.confkv_prefill(None, None, None, 0, None, None) == pkg.ERR_INVALID_ARG
     assert lib.confkv_stats(None, None) == pkg.ERR_INVALID_ARG
     assert lib.confkv_last_error(None) == b"null context"
+    assert lib.confkv_attention_path(None) == pkg.ERR_INVALID_ARG
     lib.confkv_free(None)
 
 

@@ -241,3 +241,14 @@ def test_window_full_kv_configuration():
     w = small(L=2, B=2, prefill=100, steps=40, N_high=160, N_low=160, P=8, W=160, V=64)
     rep = _check(parity.run(w, policy=1), min_frac=1.0)
     assert rep.stats["tokens_evicted"] == 0 and rep.stats["tokens_quantized"] == 0
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_attention_path_reported(d):
+    import confidence_gated_kv_logits_gb300 as pkg
+    w = small(d=d)
+    for kw, want in ((dict(), "tensor-core TMA"), (dict(attn_tma=-1), "tensor-core cp.async"),
+                     (dict(attn_kernel=1), "cuda-core")):
+        kv = pkg.ConfKV.for_workload(w, device=0, **kw)
+        assert kv.attention_path() == want
+        kv.close()
