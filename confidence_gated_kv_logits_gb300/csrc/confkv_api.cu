@@ -27,6 +27,7 @@ constexpr int kSmCount = 152;
 // 128, 4 at head_dim 64
 int attn_ctas_per_sm(int d) { return d == 64 ? 4 : 3; }
 constexpr int kProfKernels = 4;
+constexpr int kHostGroups = 2;   // most attention launches of one host step
 // "select" covers ranking, eviction, compaction moves and INT8 aging; slot 2
 // is unused (kept so that the kernel mask bits stay stable).
 const char* const kProfNames[kProfKernels] = {"confidence", "select", "append", "attention"};
@@ -81,6 +82,11 @@ struct confkv_ctx {
   int32_t* st_kc = nullptr;
   float* st_conf = nullptr;
   int32_t* st_bud = nullptr;
+  // copy stream and events of confkv_step_host (created with the staging):
+  // [0] call start, [1] selection done, [2 + g] inputs of range g on the
+  // device, [2 + kHostGroups + g] attention of range g done
+  cudaStream_t cp_stream = nullptr;
+  cudaEvent_t cp_ev[2 + 2 * kHostGroups] = {};
   std::string msg = "ok";
   alignas(64) unsigned char tmaps[confkv::kTmaMapsBytes];          // tensor maps of the d = 128 TMA path
   bool has_tmaps = false;
@@ -111,6 +117,9 @@ cudaError_t dalloc(confkv_ctx* c, T** p, size_t count) {
 void free_all(confkv_ctx* c) {
   for (void* p : c->allocs) cudaFree(p);
   c->allocs.clear();
+  for (cudaEvent_t& e : c->cp_ev)
+    if (e) { cudaEventDestroy(e); e = nullptr; }
+  if (c->cp_stream) { cudaStreamDestroy(c->cp_stream); c->cp_stream = nullptr; }
   for (int k = 0; k < kProfKernels; ++k) {
     for (cudaEvent_t e : c->ev[k]) cudaEventDestroy(e);
     c->ev[k].clear();
@@ -423,6 +432,29 @@ int run_attention_timed(confkv_ctx* c, const uint16_t* q, float* out, cudaStream
   return rc;
 }
 
+// The (layer, sequence) lanes of a host step cut into consecutive ranges,
+// one attention launch each: cuts[0] = 0 < ... < cuts[G] = L*B; returns G.
+// The outputs of range 0 are copied back while range 1 computes, so the
+// exposed copy is range 1's; a launch boundary costs about one partial wave,
+// so there are two ranges, the first ending on a whole CTA wave near 78% of
+// the step (the output copy runs at ~0.3x the attention's rate per lane).
+// Steps of fewer than 6 waves run as one launch.
+int host_ranges(const confkv_ctx* c, size_t* cuts) {
+  const size_t LB = static_cast<size_t>(c->L) * c->B;
+  const size_t per_lane = static_cast<size_t>(c->Hkv) * c->splits;        // CTAs
+  const size_t wave = static_cast<size_t>(attn_ctas_per_sm(c->d)) * kSmCount;
+  const double waves = static_cast<double>(LB * per_lane) / static_cast<double>(wave);
+  cuts[0] = 0;
+  if (waves < 6.0 || LB < 2) {
+    cuts[1] = LB;
+    return 1;
+  }
+  const size_t w0 = static_cast<size_t>(waves * 0.78 + 0.5);
+  cuts[1] = std::max<size_t>(1, std::min(LB - 1, w0 * wave / per_lane));
+  cuts[2] = LB;
+  return 2;
+}
+
 }  // namespace
 
 extern "C" {
@@ -514,6 +546,8 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
   if (!c) return CONFKV_ERR_INVALID_ARG;
   if ((!logits && uses_confidence(c)) || !q || !k_new || !v_new || !out)
     return fail(c, CONFKV_ERR_INVALID_ARG, "null logits, q, k_new, v_new or out");
+  if (c->step_open) return fail(c, CONFKV_ERR_STATE, "a per-layer step is open");
+  if (c->t >= 0x7fffffffLL) return fail(c, CONFKV_ERR_STATE, "position overflow");
   DeviceGuard guard(c->device);
   const size_t LB = static_cast<size_t>(c->L) * c->B;
   const size_t nlog = static_cast<size_t>(c->B) * c->V, nq = LB * c->Hq * c->d,
@@ -531,25 +565,86 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     A(dalloc(c, &c->st_conf, c->B));
     A(dalloc(c, &c->st_bud, c->B));
     if (e != cudaSuccess) return fail(c, e == cudaErrorMemoryAllocation ? CONFKV_ERR_OOM : CONFKV_ERR_CUDA, "staging allocation");
+    A(cudaStreamCreateWithFlags(&c->cp_stream, cudaStreamNonBlocking));
+    for (cudaEvent_t& ev : c->cp_ev) A(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("copy stream: ") + cudaGetErrorString(e));
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t cs = c->cp_stream;
+  size_t cuts[kHostGroups + 1];
+  const int G = host_ranges(c, cuts);
+  cudaEvent_t ev_start = c->cp_ev[0], ev_sel = c->cp_ev[1];
+  const cudaEvent_t* ev_in = c->cp_ev + 2;
+  const cudaEvent_t* ev_out = c->cp_ev + 2 + kHostGroups;
+  // the logits first (the confidence waits for them); q, k_new and v_new
+  // follow range by range on the copy stream (after the work already on
+  // `stream`) while the confidence and the selection run: neither reads them
+  A(cudaEventRecord(ev_start, s));
   if (logits) A(cudaMemcpyAsync(c->st_logits, logits, nlog * sizeof(float), cudaMemcpyHostToDevice, s));
-  A(cudaMemcpyAsync(c->st_q, q, nq * 2, cudaMemcpyHostToDevice, s));
-  A(cudaMemcpyAsync(c->st_k, k_new, nkv * 2, cudaMemcpyHostToDevice, s));
-  A(cudaMemcpyAsync(c->st_v, v_new, nkv * 2, cudaMemcpyHostToDevice, s));
+  A(cudaStreamWaitEvent(cs, ev_start, 0));
+  for (int gi = 0; gi < G; ++gi) {
+    const size_t lb0 = cuts[gi], nlb = cuts[gi + 1] - lb0;
+    const size_t oq = lb0 * c->Hq * c->d, okv = lb0 * c->Hkv * c->d;
+    A(cudaMemcpyAsync(c->st_q + oq, q + oq, nlb * c->Hq * c->d * 2, cudaMemcpyHostToDevice, cs));
+    A(cudaMemcpyAsync(c->st_k + okv, k_new + okv, nlb * c->Hkv * c->d * 2, cudaMemcpyHostToDevice, cs));
+    A(cudaMemcpyAsync(c->st_v + okv, v_new + okv, nlb * c->Hkv * c->d * 2, cudaMemcpyHostToDevice, cs));
+    A(cudaEventRecord(ev_in[gi], cs));
+  }
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("H2D: ") + cudaGetErrorString(e));
-  const int rc = confkv_step(c, logits ? c->st_logits : nullptr, c->st_q, c->st_k, c->st_v, c->st_out,
-                             kept_pos ? c->st_kp : nullptr, kept_count ? c->st_kc : nullptr,
-                             conf_out ? c->st_conf : nullptr, budget_out ? c->st_bud : nullptr,
-                             stream);
+  int rc;
+  if (uses_confidence(c)) {
+    rc = run_confidence(c, c->st_logits, conf_out ? c->st_conf : nullptr,
+                        budget_out ? c->st_bud : nullptr, s);
+    if (rc != CONFKV_OK) return rc;
+  }
+  // the selection of every (layer, sequence), reserving the new tokens'
+  // slots; the kept lists are final here and go back during the attention
+  int32_t* kp = kept_pos ? c->st_kp : nullptr;
+  int32_t* kc = kept_count ? c->st_kc : nullptr;
+  StepParams sel = step_params(c, 0, static_cast<int>(LB), nullptr, nullptr, kp, kc);
+  sel.defer_new = 1;
+  rc = run_select(c, sel, s);
   if (rc != CONFKV_OK) return rc;
-  A(cudaMemcpyAsync(out, c->st_out, nq * sizeof(float), cudaMemcpyDeviceToHost, s));
-  if (kept_pos) A(cudaMemcpyAsync(kept_pos, c->st_kp, nkp * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
-  if (kept_count) A(cudaMemcpyAsync(kept_count, c->st_kc, LB * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  A(cudaEventRecord(ev_sel, s));
+  A(cudaStreamWaitEvent(cs, ev_sel, 0));
+  if (kept_pos)
+    A(cudaMemcpyAsync(kept_pos, c->st_kp, nkp * sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+  if (kept_count)
+    A(cudaMemcpyAsync(kept_count, c->st_kc, LB * sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
   if (conf_out && uses_confidence(c))
-    A(cudaMemcpyAsync(conf_out, c->st_conf, c->B * sizeof(float), cudaMemcpyDeviceToHost, s));
+    A(cudaMemcpyAsync(conf_out, c->st_conf, c->B * sizeof(float), cudaMemcpyDeviceToHost, cs));
   if (budget_out && uses_confidence(c))
-    A(cudaMemcpyAsync(budget_out, c->st_bud, c->B * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    A(cudaMemcpyAsync(budget_out, c->st_bud, c->B * sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+  const bool fused = confkv::attention_uses_mma(c->cache, c->attn_kernel);
+  if (!fused) {
+    A(cudaStreamWaitEvent(s, ev_in[G - 1], 0));
+    const StepParams ap = step_params(c, 0, static_cast<int>(LB), c->st_k, c->st_v, nullptr, nullptr);
+    prof_mark(c, 2, s);
+    A(confkv::launch_append(c->cache, ap, s));
+    prof_mark(c, 2, s);
+    if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("append: ") + cudaGetErrorString(e));
+  }
+  // one attention launch per range, as soon as its inputs are on the device;
+  // its outputs go back on the copy stream while the next range computes
+  for (int gi = 0; gi < G; ++gi) {
+    const size_t lb0 = cuts[gi], nlb = cuts[gi + 1] - lb0;
+    A(cudaStreamWaitEvent(s, ev_in[gi], 0));
+    const StepParams f = step_params(c, static_cast<int>(lb0), static_cast<int>(nlb),
+                                     c->st_k + lb0 * c->Hkv * c->d, c->st_v + lb0 * c->Hkv * c->d,
+                                     nullptr, nullptr);
+    rc = run_attention_timed(c, c->st_q + lb0 * c->Hq * c->d, c->st_out + lb0 * c->Hq * c->d, s,
+                             static_cast<int>(lb0), static_cast<int>(nlb), c->splits,
+                             fused ? &f : nullptr);
+    if (rc != CONFKV_OK) return rc;
+    A(cudaEventRecord(ev_out[gi], s));
+    A(cudaStreamWaitEvent(cs, ev_out[gi], 0));
+    const size_t oq = lb0 * c->Hq * c->d;
+    A(cudaMemcpyAsync(out + oq, c->st_out + oq, nlb * c->Hq * c->d * sizeof(float),
+                      cudaMemcpyDeviceToHost, cs));
+  }
+  c->t += 1;
+  c->steps += 1;
+  A(cudaStreamSynchronize(cs));
   A(cudaStreamSynchronize(s));
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("D2H: ") + cudaGetErrorString(e));
   return CONFKV_OK;
