@@ -243,7 +243,8 @@ int confkv_step_layer(confkv_ctx* ctx, int layer, const uint16_t* q, const uint1
  * outputs are skipped.  The results equal confkv_step's bit for bit, except
  * that kept_pos entries past kept_count are unspecified here (the whole
  * staging row is copied back).  The call synchronises, so it cannot be
- * captured in a CUDA graph.
+ * captured in a CUDA graph.  The first call allocates the staging buffers
+ * (the inputs' and outputs' sizes), a copy stream and its events.
  */
 int confkv_step_host(confkv_ctx* ctx, const float* logits, const uint16_t* q,
                      const uint16_t* k_new, const uint16_t* v_new, float* out,
