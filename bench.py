@@ -56,6 +56,10 @@ def parse():
     p.add_argument("--step-bytes", action="store_true",
                    help="profiling only: run warmup+steps decode steps and print each "
                         "step's algorithmic attention bytes (synchronises every step)")
+    p.add_argument("--per-layer", action="store_true",
+                   help="time the per-layer entry points instead (confkv_step_begin + one "
+                        "confkv_step_layer per layer, captured once in a CUDA graph and "
+                        "replayed as every step); prints its own JSON line")
     return p.parse_args()
 
 
@@ -596,12 +600,99 @@ def run_step_bytes(args):
     return 0
 
 
+def run_per_layer(args):
+    """Per-layer stepping: each step is confkv_step_begin (confidence and the
+    selection of every layer) followed by confkv_step_layer for every layer
+    (the new token's K/V store and that layer's attention), as a model that
+    produces each layer's query after the previous layer's attention calls it.
+    One such step is captured in a CUDA graph and replayed as every step, the
+    step's inputs copied (device to device) into the captured buffers first;
+    both are inside the timed region."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import confidence_gated_kv_logits_gb300 as pkg
+    from synth import device as sd, workloads as wl
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = get_workload(args)
+    K, Wm = args.steps, args.warmup
+    S = K + Wm + 1
+    kv = pkg.ConfKV.for_workload(w)
+    if w.prefill:
+        Kp, Vp = sd.prefill_kv(w)
+        ql = wl.q_last(w)
+        kv.prefill(Kp, Vp, w.prefill, None if ql is None else torch.from_numpy(ql).to(dev))
+        torch.cuda.synchronize()
+        del Kp, Vp
+        torch.cuda.empty_cache()
+    LG = torch.empty(S, w.B, w.V, dtype=torch.float32, device=dev)
+    Q = torch.empty(S, w.L, w.B, w.Hq, w.d, dtype=torch.float16, device=dev)
+    KN = torch.empty(S, w.L, w.B, w.Hkv, w.d, dtype=torch.float16, device=dev)
+    VN = torch.empty(S, w.L, w.B, w.Hkv, w.d, dtype=torch.float16, device=dev)
+    for s in range(S):
+        sd.step_inputs(w, s, (LG[s], Q[s], KN[s], VN[s]))
+    lg, q, k, v = (torch.empty_like(x[0]) for x in (LG, Q, KN, VN))
+    out = torch.empty(w.L, w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+    kp = torch.empty(w.L, w.B, kv.Ncap, dtype=torch.int32, device=dev)
+    kc = torch.empty(w.L, w.B, dtype=torch.int32, device=dev)
+
+    def load(s):
+        for dst, src in zip((lg, q, k, v), (LG[s], Q[s], KN[s], VN[s])):
+            dst.copy_(src)
+
+    def one(stream=None):
+        kv.step_begin(lg, stream=stream)
+        for l in range(w.L):
+            kv.step_layer(l, q[l], k[l], v[l], out[l], kp[l], kc[l], stream=stream)
+
+    load(0)
+    one()                                     # step 0 eagerly
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    load(1)
+    with torch.cuda.graph(g, stream=cap):
+        one(cap)                              # capturing enqueues nothing
+    torch.cuda.synchronize()
+    for s in range(1, 1 + Wm):
+        load(s)
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(1 + Wm, 1 + Wm + K):
+        load(s)
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    st, rc = kv.stats()
+    line = {"metric": "decode tokens/s on 1 GB300 (full CONF-KV step, per-layer entry points)",
+            "value": w.B / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K,
+            "warmup": Wm, "ms_per_step": ms, "higher_is_better": True,
+            "config": {"workload": w.name, "layers": w.L, "batch": w.B,
+                       "attn_splits_per_layer": "automatic",
+                       "attention": kv.attention_path()},
+            "note": "confkv_step_begin + %d x confkv_step_layer per step, one CUDA graph "
+                    "replayed per step after a device-to-device copy of the step's inputs "
+                    "into the captured buffers (both timed)" % w.L,
+            "steps_on_device": st["steps"], "status": rc}
+    print(json.dumps(line), flush=True)
+    kv.close()
+    return 0 if rc == 0 else 1
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.step_bytes:
         return run_step_bytes(args)
+    if args.per_layer:
+        return run_per_layer(args)
     return run_ours(args)
 
 
