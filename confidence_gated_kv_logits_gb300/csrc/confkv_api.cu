@@ -87,6 +87,7 @@ struct confkv_ctx {
   // device, [2 + kHostGroups + g] attention of range g done
   cudaStream_t cp_stream = nullptr;
   cudaEvent_t cp_ev[2 + 2 * kHostGroups] = {};
+  bool cp_ready = false;
   std::string msg = "ok";
   alignas(64) unsigned char tmaps[confkv::kTmaMapsBytes];          // tensor maps of the d = 128 TMA path
   bool has_tmaps = false;
@@ -120,6 +121,7 @@ void free_all(confkv_ctx* c) {
   for (cudaEvent_t& e : c->cp_ev)
     if (e) { cudaEventDestroy(e); e = nullptr; }
   if (c->cp_stream) { cudaStreamDestroy(c->cp_stream); c->cp_stream = nullptr; }
+  c->cp_ready = false;
   for (int k = 0; k < kProfKernels; ++k) {
     for (cudaEvent_t e : c->ev[k]) cudaEventDestroy(e);
     c->ev[k].clear();
@@ -565,12 +567,23 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     A(dalloc(c, &c->st_conf, c->B));
     A(dalloc(c, &c->st_bud, c->B));
     if (e != cudaSuccess) return fail(c, e == cudaErrorMemoryAllocation ? CONFKV_ERR_OOM : CONFKV_ERR_CUDA, "staging allocation");
-    A(cudaStreamCreateWithFlags(&c->cp_stream, cudaStreamNonBlocking));
-    for (cudaEvent_t& ev : c->cp_ev) A(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+  }
+  if (!c->cp_ready) {
+    if (!c->cp_stream) A(cudaStreamCreateWithFlags(&c->cp_stream, cudaStreamNonBlocking));
+    for (cudaEvent_t& ev : c->cp_ev)
+      if (!ev) A(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
     if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("copy stream: ") + cudaGetErrorString(e));
+    c->cp_ready = true;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaStream_t cs = c->cp_stream;
+  // once copies are enqueued, no return may leave one in flight (the
+  // caller's host buffers are only borrowed for the call)
+  auto drain = [&](int code) {
+    cudaStreamSynchronize(cs);
+    cudaStreamSynchronize(s);
+    return code;
+  };
   size_t cuts[kHostGroups + 1];
   const int G = host_ranges(c, cuts);
   cudaEvent_t ev_start = c->cp_ev[0], ev_sel = c->cp_ev[1];
@@ -590,12 +603,12 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     A(cudaMemcpyAsync(c->st_v + okv, v_new + okv, nlb * c->Hkv * c->d * 2, cudaMemcpyHostToDevice, cs));
     A(cudaEventRecord(ev_in[gi], cs));
   }
-  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("H2D: ") + cudaGetErrorString(e));
+  if (e != cudaSuccess) return drain(fail(c, CONFKV_ERR_CUDA, std::string("H2D: ") + cudaGetErrorString(e)));
   int rc;
   if (uses_confidence(c)) {
     rc = run_confidence(c, c->st_logits, conf_out ? c->st_conf : nullptr,
                         budget_out ? c->st_bud : nullptr, s);
-    if (rc != CONFKV_OK) return rc;
+    if (rc != CONFKV_OK) return drain(rc);
   }
   // the selection of every (layer, sequence), reserving the new tokens'
   // slots; the kept lists are final here and go back during the attention
@@ -604,7 +617,7 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
   StepParams sel = step_params(c, 0, static_cast<int>(LB), nullptr, nullptr, kp, kc);
   sel.defer_new = 1;
   rc = run_select(c, sel, s);
-  if (rc != CONFKV_OK) return rc;
+  if (rc != CONFKV_OK) return drain(rc);
   A(cudaEventRecord(ev_sel, s));
   A(cudaStreamWaitEvent(cs, ev_sel, 0));
   if (kept_pos)
@@ -622,7 +635,7 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     prof_mark(c, 2, s);
     A(confkv::launch_append(c->cache, ap, s));
     prof_mark(c, 2, s);
-    if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("append: ") + cudaGetErrorString(e));
+    if (e != cudaSuccess) return drain(fail(c, CONFKV_ERR_CUDA, std::string("append: ") + cudaGetErrorString(e)));
   }
   // one attention launch per range, as soon as its inputs are on the device;
   // its outputs go back on the copy stream while the next range computes
@@ -635,7 +648,7 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     rc = run_attention_timed(c, c->st_q + lb0 * c->Hq * c->d, c->st_out + lb0 * c->Hq * c->d, s,
                              static_cast<int>(lb0), static_cast<int>(nlb), c->splits,
                              fused ? &f : nullptr);
-    if (rc != CONFKV_OK) return rc;
+    if (rc != CONFKV_OK) return drain(rc);
     A(cudaEventRecord(ev_out[gi], s));
     A(cudaStreamWaitEvent(cs, ev_out[gi], 0));
     const size_t oq = lb0 * c->Hq * c->d;

@@ -102,13 +102,13 @@ def test_per_layer_state_errors():
     kv.close()
 
 
-def _eager_and_graph(w, per_layer, n_eager, n_replay):
+def _eager_and_graph(w, per_layer, n_eager, n_replay, policy=0):
     """Runs n_eager eager steps, then n_replay more either eagerly or as
     replays of one captured step; returns the last outputs of each run."""
     import confidence_gated_kv_logits_gb300 as pkg
     results = []
     for graph in (False, True):
-        kv = pkg.ConfKV.for_workload(w, device=0)
+        kv = pkg.ConfKV.for_workload(w, device=0, policy=policy, seed=11)
         kvs = [[wl.prefill_kv_lb(w, l, bb) for bb in range(w.B)] for l in range(w.L)]
         K = np.stack([np.stack([x[0] for x in row]) for row in kvs])
         V = np.stack([np.stack([x[1] for x in row]) for row in kvs])
@@ -165,13 +165,15 @@ def _eager_and_graph(w, per_layer, n_eager, n_replay):
     return results
 
 
-@pytest.mark.parametrize("per_layer", [False, True])
-def test_step_graph_replayed_equals_eager(per_layer):
+@pytest.mark.parametrize("per_layer,policy", [(False, 0), (True, 0), (False, 1), (True, 3),
+                                              (False, 2)])
+def test_step_graph_replayed_equals_eager(per_layer, policy):
     # one captured step replayed for several decode steps (new inputs written
     # into the captured buffers before each replay) gives the same bits as
-    # the same steps run eagerly: the position and all state are on the device
+    # the same steps run eagerly: the position and all state are on the
+    # device (policy 3 draws its keys from the position; 1 has no confidence)
     w = small(L=3, B=2, steps=20)
-    eager, graph = _eager_and_graph(w, per_layer, n_eager=4, n_replay=14)
+    eager, graph = _eager_and_graph(w, per_layer, n_eager=4, n_replay=14, policy=policy)
     for a, b in zip(eager, graph):
         if a.dtype == np.float32:
             a, b = a.view(np.uint32), b.view(np.uint32)
