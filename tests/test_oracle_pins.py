@@ -261,3 +261,42 @@ def test_attention_special_cases():
     assert np.allclose(prob, 1 / 6) and np.allclose(out, v.mean(0), atol=1e-14)
     out, prob = oracle.attention_head(rng.standard_normal(16), np.ones((1, 16)), v[:1])
     assert prob[0] == 1.0 and np.array_equal(out, v[0])
+
+
+def _printed_constants():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "conf_kv_printed_constants.txt")
+    out = {}
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, value = line.split()[:2]
+        out[key] = value
+    return out
+
+
+@pytest.mark.parametrize("a", [0.0, 0.7, 2.5, -4.0])
+def test_confidence_uses_the_printed_weights(a):
+    # the weights as the pages print them (golden fixture), applied to the
+    # two-token closed form: p = sigma(|a|), H^ = h2(p) / ln 2, m = |a|
+    k = _printed_constants()
+    w1, w2, w3 = (float(k[x]) for x in ("weight_one_minus_entropy", "weight_sigma_margin",
+                                        "weight_top1_probability"))
+    assert abs(w1 + w2 + w3 - 1.0) < 1e-15
+    af = float(np.float32(a))
+    p = 1.0 / (1.0 + math.exp(-abs(af)))
+    h2 = -(p * math.log(p) + (1 - p) * math.log(1 - p))
+    want = w1 * (1 - h2 / math.log(2.0)) + w2 * p + w3 * p
+    c = oracle.confidence(np.array([af, 0.0], dtype=np.float32))[0]
+    assert abs(c - want) < 1e-13
+
+
+def test_budget_rule_as_printed():
+    # c >= tau -> the tight budget N_high; c < tau -> N_low (golden fixture)
+    assert _printed_constants()["high_confidence_rule"] == "ge"
+    z = np.array([math.log(3.0), 0.0], dtype=np.float32)
+    c = np.float32(oracle.confidence(z)[0])          # c and tau compare in fp32
+    assert oracle.budget(c, tau=c, n_low=64, n_high=16) == 16
+    above = np.nextafter(c, np.float32(2.0))
+    assert oracle.budget(c, tau=above, n_low=64, n_high=16) == 64
