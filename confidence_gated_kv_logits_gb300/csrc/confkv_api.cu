@@ -89,7 +89,7 @@ struct confkv_ctx {
   cudaEvent_t cp_ev[2 + 2 * kHostGroups] = {};
   bool cp_ready = false;
   std::string msg = "ok";
-  alignas(64) unsigned char tmaps[confkv::kTmaMapsBytes];          // tensor maps of the d = 128 TMA path
+  alignas(64) unsigned char tmaps[confkv::kTmaMapsBytes];          // tensor maps of the TMA attention path
   bool has_tmaps = false;
   // profiling
   int prof = 0;                                 // kernel bit mask

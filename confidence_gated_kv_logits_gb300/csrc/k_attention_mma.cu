@@ -23,9 +23,12 @@
 // contiguous slice of a K row (32 B of INT8 at d = 128); the M index of the
 // P.V product is permuted so that each thread reads one contiguous slice of
 // a V row.  Each warp streams its own chunks (32 INT8 tokens or 16 FP16
-// tokens, 8 KB at d = 128) through a cp.async ring of kStages stages in a
-// thread-private shared-memory layout (conflict-free, no cross-lane data
-// except the 64 scales of an INT8 chunk).
+// tokens, 8 KB at d = 128) through a ring of kStages stages: by default
+// 2-D TMA boxes into swizzled tiles (128-byte swizzle; 64-byte for the
+// 64-byte INT8 rows of d = 64), each stage completing an mbarrier with a
+// bounded wait; or (attn_tma = -1) per-lane cp.async into a thread-private
+// layout (conflict-free, no cross-lane data except the 64 scales of an INT8
+// chunk).
 //
 // Split-K: with 2..8 splits the splits of a unit form one thread-block
 // cluster and merge through distributed shared memory: after a cluster
