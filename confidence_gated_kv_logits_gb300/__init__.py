@@ -34,7 +34,18 @@ EXPORTS = ("confkv_create", "confkv_prefill", "confkv_step", "confkv_step_host",
            "confkv_stats", "confkv_read_cache", "confkv_profile_enable",
            "confkv_profile_read", "confkv_last_error", "confkv_free",
            "confkv_confidence_noalloc", "confkv_step_begin", "confkv_step_layer",
-           "confkv_attention_path")
+           "confkv_attention_path", "confkv_selftest_bounded_wait")
+
+
+def selftest_bounded_wait(device=0, timeout_us=1000):
+    """Runs confkv_selftest_bounded_wait; returns (gave_up, waited_us)."""
+    L = load_library()
+    g = ctypes.c_int()
+    w = ctypes.c_double()
+    rc = L.confkv_selftest_bounded_wait(int(device), int(timeout_us), ctypes.byref(g), ctypes.byref(w))
+    if rc != OK:
+        raise ConfKVError(rc, "bounded-wait self-test")
+    return bool(g.value), w.value
 
 
 class ConfKVError(RuntimeError):
@@ -106,6 +117,8 @@ def load_library(path=LIB_PATH):
     L.confkv_last_error.argtypes = [vp]
     L.confkv_free.restype = None
     L.confkv_free.argtypes = [vp]
+    L.confkv_selftest_bounded_wait.restype = ci
+    L.confkv_selftest_bounded_wait.argtypes = [ci, ci, ctypes.POINTER(ci), ctypes.POINTER(ctypes.c_double)]
     L.confkv_attention_path.restype = ci
     L.confkv_attention_path.argtypes = [vp]
     L.confkv_confidence_noalloc.restype = ci

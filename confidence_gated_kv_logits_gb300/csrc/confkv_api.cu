@@ -798,6 +798,26 @@ int confkv_profile_read(confkv_ctx* c, confkv_profile_t* out) {
   return CONFKV_OK;
 }
 
+int confkv_selftest_bounded_wait(int device, int timeout_us, int* gave_up, double* waited_us) {
+  if (!gave_up || !waited_us || timeout_us < 1 || timeout_us > 1000000) return CONFKV_ERR_INVALID_ARG;
+  DeviceGuard guard(device);
+  void* buf = nullptr;
+  if (cudaMalloc(&buf, 16) != cudaSuccess) return CONFKV_ERR_CUDA;
+  unsigned long long* d_ns = static_cast<unsigned long long*>(buf);
+  int* d_flag = reinterpret_cast<int*>(d_ns + 1);
+  cudaError_t e = confkv::selftest_bounded_wait(static_cast<unsigned long long>(timeout_us) * 1000ull,
+                                                d_flag, d_ns, nullptr);
+  unsigned long long ns = 0;
+  int flag = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&ns, d_ns, sizeof(ns), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&flag, d_flag, sizeof(flag), cudaMemcpyDeviceToHost);
+  cudaFree(buf);
+  if (e != cudaSuccess) return CONFKV_ERR_CUDA;
+  *gave_up = flag;
+  *waited_us = static_cast<double>(ns) * 1e-3;
+  return CONFKV_OK;
+}
+
 int confkv_attention_path(const confkv_ctx* c) {
   if (!c) return CONFKV_ERR_INVALID_ARG;
   if (!confkv::attention_uses_mma(c->cache, c->attn_kernel)) return CONFKV_ATTN_CUDA_CORE;

@@ -168,5 +168,10 @@ cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStrea
 // or the cache is too large for 32-bit tile coordinates.
 constexpr int kTmaMapsBytes = 512;
 bool encode_attention_maps(const Cache& c, void* out);
+// One thread waits, with the attention's bounded mbarrier wait and limit
+// limit_ns, on a phase nothing completes; *gave_up = 1 when it gave up,
+// *waited_ns the device time it waited (device pointers).
+cudaError_t selftest_bounded_wait(unsigned long long limit_ns, int* gave_up,
+                                  unsigned long long* waited_ns, cudaStream_t s);
 
 }  // namespace confkv

@@ -160,7 +160,10 @@ template <int D>
 constexpr int kTmaTile = 32 * D;
 template <int D>
 constexpr int kTmaStage = (D == 128) ? 9216 : 5120;
-constexpr unsigned kWaitSpins = 1u << 26;        // bounded mbarrier wait (then flag + bail)
+// Bounded mbarrier wait: give up (the caller flags it and bails out) after
+// kWaitNs of device time or kWaitSpins polls, whichever comes first.
+constexpr unsigned kWaitSpins = 1u << 26;
+constexpr unsigned long long kWaitNs = 2000000000ull;      // 2 s
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
@@ -179,10 +182,21 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, unsigned parity) {
       : "memory");
   return ok != 0;
 }
-// bounded wait: false when the copy never completed (the caller flags it)
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, unsigned parity) {
-  for (unsigned i = 0; i < kWaitSpins; ++i)
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+// bounded wait: false when the phase never completed within limit_ns (the
+// caller flags it)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, unsigned parity,
+                                          unsigned long long limit_ns = kWaitNs) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (unsigned i = 1; i < kWaitSpins; ++i) {
     if (mbar_try(bar, parity)) return true;
+    if ((i & 31u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+  }
   return false;
 }
 // L2 policy for the streamed K/V tiles: evict first, so that the scores and
@@ -914,6 +928,20 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   }
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier phase that
+// nothing will complete (its one expected arrival never comes) and records
+// whether the wait gave up and after how long.
+__global__ void k_selftest_wait(unsigned long long limit_ns, int* gave_up, unsigned long long* waited_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  const unsigned long long t0 = globaltimer_ns();
+  const bool ok = mbar_wait(b, 0, limit_ns);
+  *waited_ns = globaltimer_ns() - t0;
+  *gave_up = ok ? 0 : 1;
+}
+
 template <int D, bool TMA>
 cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm, cudaStream_t s) {
   const int smem = kWarps * kStages * (TMA ? kTmaStage<D> : Geo<D>::STAGE) + (TMA ? 1024 : 0);
@@ -1041,6 +1069,12 @@ cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStrea
     return launch_mma_d<128, false>(c, ap, tm, s);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t selftest_bounded_wait(unsigned long long limit_ns, int* gave_up,
+                                  unsigned long long* waited_ns, cudaStream_t s) {
+  k_selftest_wait<<<1, 1, 0, s>>>(limit_ns, gave_up, waited_ns);
+  return cudaGetLastError();
 }
 
 }  // namespace confkv

@@ -325,6 +325,19 @@ int confkv_confidence_noalloc(const float* logits, int batch, int vocab, float t
 #define CONFKV_ATTN_TENSOR_TMA 2
 int confkv_attention_path(const confkv_ctx* ctx);
 
+/*
+ * confkv_selftest_bounded_wait -- checks the device-side failure path of the
+ * attention's tile waits without any fault: on `device`, one thread waits
+ * with the same bounded mbarrier wait, limited to `timeout_us`, on a phase
+ * that nothing completes.  *gave_up receives 1 when the wait gave up (the
+ * expected result), *waited_us the device time it waited.  Synchronous;
+ * allocates 16 bytes of device memory for the call.  timeout_us must be in
+ * [1, 1000000], else CONFKV_ERR_INVALID_ARG; CONFKV_ERR_CUDA on a CUDA error.
+ * The attention kernel's own limit is 2 s per wait, after which it flags
+ * CONFKV_FLAG_TIMEOUT (returned by confkv_stats) and leaves the unit.
+ */
+int confkv_selftest_bounded_wait(int device, int timeout_us, int* gave_up, double* waited_us);
+
 /* Message of the last error of this context (never NULL). */
 const char* confkv_last_error(const confkv_ctx* ctx);
 

@@ -72,6 +72,10 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.confkv_stats(None, None) == pkg.ERR_INVALID_ARG
     assert lib.confkv_last_error(None) == b"null context"
     assert lib.confkv_attention_path(None) == pkg.ERR_INVALID_ARG
+    g, w = ctypes.c_int(), ctypes.c_double()
+    assert lib.confkv_selftest_bounded_wait(0, 0, ctypes.byref(g), ctypes.byref(w)) == pkg.ERR_INVALID_ARG
+    assert lib.confkv_selftest_bounded_wait(0, 2000000, ctypes.byref(g), ctypes.byref(w)) == pkg.ERR_INVALID_ARG
+    assert lib.confkv_selftest_bounded_wait(0, 100, None, ctypes.byref(w)) == pkg.ERR_INVALID_ARG
     lib.confkv_free(None)
 
 

@@ -252,3 +252,14 @@ def test_attention_path_reported(d):
         kv = pkg.ConfKV.for_workload(w, device=0, **kw)
         assert kv.attention_path() == want
         kv.close()
+
+
+def test_bounded_wait_gives_up_and_device_stays_usable():
+    # the attention's tile wait on a phase that nothing completes gives up
+    # after its limit (no fault, no hang), and the GPU keeps working
+    import confidence_gated_kv_logits_gb300 as pkg
+    gave_up, waited_us = pkg.selftest_bounded_wait(0, timeout_us=2000)
+    assert gave_up
+    assert 2000.0 <= waited_us < 200000.0
+    w = small(steps=6)
+    _check(parity.run(w))
