@@ -185,13 +185,15 @@ int auto_splits(int units, int ncap, int d) {
   return floor_pow2(std::max(1, std::min(std::min(want, tok_lim), 8)));
 }
 
-// One layer's launch holds few units, so its time is one CTA's latency: about
-// two CTAs per SM, same token floor, cap and rounding (Qwen-32B shape, 64
-// units per layer: 4 splits 14.4 us per layer, 8 splits 21.6 us).
-int auto_splits_layer(int units, int ncap) {
-  const int want = std::max(1, 2 * kSmCount / units);
-  const int tok_lim = std::max(1, (ncap + 1) / 512);
-  return floor_pow2(std::max(1, std::min(std::min(want, tok_lim), 8)));
+// One layer's launch holds few units, so its time is one CTA's latency: as
+// many splits as still fit one wave, at least ~256 budget tokens per split,
+// at most 8, an even count (Qwen-32B shape, 64 units per layer, per-layer
+// step: 4 splits 927 us, 5: 883, 6: 884, 7: 1403 -- a 7-CTA cluster).
+int auto_splits_layer(int units, int ncap, int d) {
+  const int want = std::max(1, attn_ctas_per_sm(d) * kSmCount / units);
+  const int tok_lim = std::max(1, (ncap + 1) / 256);
+  const int n = std::max(1, std::min(std::min(want, tok_lim), 8));
+  return n > 1 ? (n & ~1) : 1;
 }
 
 int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s, int lb0, int nlb,
@@ -284,7 +286,7 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
     c->splits = c->splits_layer = o.attn_splits;
   } else {
     c->splits = auto_splits(units, c->Ncap, c->d);
-    c->splits_layer = auto_splits_layer(c->B * c->Hkv, c->Ncap);
+    c->splits_layer = auto_splits_layer(c->B * c->Hkv, c->Ncap, c->d);
   }
   const int max_splits = std::max(c->splits, c->splits_layer);
 
