@@ -22,14 +22,15 @@ using confkv::StepParams;
 
 namespace {
 
-constexpr int kSmCount = 152;
+constexpr int kSmCountDefault = 152;   // GB300; the context reads the device's own count
 // resident tensor-core attention CTAs per SM (register-bound): 3 at head_dim
 // 128, 4 at head_dim 64
 int attn_ctas_per_sm(int d) { return d == 64 ? 4 : 3; }
 constexpr int kProfKernels = 4;
 constexpr int kHostGroups = 2;   // most attention launches of one host step
-// "select" covers ranking, eviction, compaction moves and INT8 aging; slot 2
-// is unused (kept so that the kernel mask bits stay stable).
+// "select" covers ranking, eviction, compaction moves and INT8 aging;
+// "append" is the arriving token's store under per-layer stepping (a kernel
+// of its own only with the CUDA-core attention).
 const char* const kProfNames[kProfKernels] = {"confidence", "select", "append", "attention"};
 
 struct DeviceGuard {
@@ -49,6 +50,7 @@ struct confkv_ctx {
   int L = 0, B = 0, Hq = 0, Hkv = 0, d = 0, g = 0, V = 0;
   int N_low = 0, N_high = 0, P = 0, W = 0, Wr = 0, Ncap = 0, cap8 = 0, slots = 0;
   int max_context = 0, device = 0, splits = 1, splits_layer = 1, attn_kernel = 0;
+  int sms = kSmCountDefault;   // the device's SM count (launch-shape heuristics)
   // per-layer stepping (confkv_step_begin / confkv_step_layer)
   bool step_open = false;
   int layers_left = 0;
@@ -179,8 +181,8 @@ int floor_pow2(int x) {
 // more than the idle SMs they would fill (Qwen-14B shape, 384 units: 1 split
 // 48 us, 2 splits 60 us; gpt-oss shape, 192 units: 2 splits 31 us, 3 splits
 // 43 us, 4 splits 39 us).
-int auto_splits(int units, int ncap, int d) {
-  const int want = std::max(1, attn_ctas_per_sm(d) * kSmCount / units);
+int auto_splits(int units, int ncap, int d, int sms) {
+  const int want = std::max(1, attn_ctas_per_sm(d) * sms / units);
   const int tok_lim = std::max(1, (ncap + 1) / 512);
   return floor_pow2(std::max(1, std::min(std::min(want, tok_lim), 8)));
 }
@@ -189,8 +191,8 @@ int auto_splits(int units, int ncap, int d) {
 // many splits as still fit one wave, at least ~256 budget tokens per split,
 // at most 8, an even count (Qwen-32B shape, 64 units per layer, per-layer
 // step: 4 splits 927 us, 5: 883, 6: 884, 7: 1403 -- a 7-CTA cluster).
-int auto_splits_layer(int units, int ncap, int d) {
-  const int want = std::max(1, attn_ctas_per_sm(d) * kSmCount / units);
+int auto_splits_layer(int units, int ncap, int d, int sms) {
+  const int want = std::max(1, attn_ctas_per_sm(d) * sms / units);
   const int tok_lim = std::max(1, (ncap + 1) / 256);
   const int n = std::max(1, std::min(std::min(want, tok_lim), 8));
   return n > 1 ? (n & ~1) : 1;
@@ -267,6 +269,13 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   c->pyramid_min = pmin;
   c->max_context = o.max_context;
   c->device = dev;
+  {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+      c->sms = sms;
+    else
+      (void)cudaGetLastError();
+  }
   c->attn_kernel = o.attn_kernel;
   c->policy = o.policy;
   c->seed = o.seed;
@@ -285,8 +294,8 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   if (o.attn_splits > 0) {
     c->splits = c->splits_layer = o.attn_splits;
   } else {
-    c->splits = auto_splits(units, c->Ncap, c->d);
-    c->splits_layer = auto_splits_layer(c->B * c->Hkv, c->Ncap, c->d);
+    c->splits = auto_splits(units, c->Ncap, c->d, c->sms);
+    c->splits_layer = auto_splits_layer(c->B * c->Hkv, c->Ncap, c->d, c->sms);
   }
   const int max_splits = std::max(c->splits, c->splits_layer);
 
@@ -446,7 +455,7 @@ int run_attention_timed(confkv_ctx* c, const uint16_t* q, float* out, cudaStream
 int host_ranges(const confkv_ctx* c, size_t* cuts) {
   const size_t LB = static_cast<size_t>(c->L) * c->B;
   const size_t per_lane = static_cast<size_t>(c->Hkv) * c->splits;        // CTAs
-  const size_t wave = static_cast<size_t>(attn_ctas_per_sm(c->d)) * kSmCount;
+  const size_t wave = static_cast<size_t>(attn_ctas_per_sm(c->d)) * c->sms;
   const double waves = static_cast<double>(LB * per_lane) / static_cast<double>(wave);
   cuts[0] = 0;
   if (waves < 6.0 || LB < 2) {
