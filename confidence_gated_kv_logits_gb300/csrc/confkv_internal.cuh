@@ -38,9 +38,13 @@ __device__ __forceinline__ void l2_discard_line(const void* p) {
 // attribute both are no-ops.  Every kernel waits before it completes, so a
 // grid's completion implies that of every earlier kernel in the stream.  The
 // confidence kernel triggers right after its own wait and the attention after
-// its main loop; the selection kernel triggers at its start, which is safe
-// because the attention reads nothing but its caller's queries before its
-// wait.
+// its main loop; the selection and append kernels trigger at their start,
+// which is safe because the attention reads nothing but its caller's queries
+// before its wait.  The selection reads the previous step's state before its
+// own wait: its predecessor is the confidence kernel (which has waited for
+// the previous attention) or, under the WINDOW policy, the previous step's
+// attention, whose trigger comes after every read of the cache data the
+// selection moves.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");

@@ -30,7 +30,12 @@
 // is one arg-min.  Keep flags become 32-bit ballot masks; one warp per region
 // turns them into the compaction plan with popc / ffs.  The same CTA then
 // applies the compaction: metadata and K/V data moves of every KV head, the
-// INT8 quantisation of the aging token and the write of the new token.
+// INT8 quantisation of the aging token and the write of the new token.  In
+// the deferred form (per-layer steps, host-buffer steps) the new token's K/V
+// rows are not yet known: the CTA only reserves their FP16 slot (new_slot)
+// and the attention, or k_append, stores them.  The step position is the
+// prefill length plus a per-(layer, sequence) device counter this kernel
+// advances, so a captured step replays as the next one.
 #include <cfloat>
 
 #include "../../include/confkv.h"
