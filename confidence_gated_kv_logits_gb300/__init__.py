@@ -136,16 +136,16 @@ def _dptr(t, dtype, numel, name, device):
     if t.dtype != dtype or not t.is_contiguous() or t.numel() != numel:
         raise ValueError(f"{name}: want contiguous {dtype} with {numel} elements, got "
                          f"{t.dtype} {tuple(t.shape)}")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _hptr(a, np_dtype, numel, name):
+    """Address of a C-contiguous numpy array (argument checks only)."""
     if a is None:
         return None
-    import numpy as np
-    if a.dtype != np_dtype or not a.flags["C_CONTIGUOUS"] or a.size != numel:
+    if a.dtype != np_dtype or not a.flags.c_contiguous or a.size != numel:
         raise ValueError(f"{name}: want C-contiguous {np_dtype} with {numel} elements")
-    return a.ctypes.data_as(ctypes.c_void_p)
+    return a.ctypes.data
 
 
 class ConfKV:
@@ -197,7 +197,7 @@ class ConfKV:
     def _stream(stream):
         import torch
         s = stream if stream is not None else torch.cuda.current_stream()
-        return ctypes.c_void_p(s.cuda_stream)
+        return s.cuda_stream
 
     def prefill(self, k, v, T, q_last=None, stream=None):
         import torch
