@@ -60,6 +60,9 @@ def parse():
                    help="time the per-layer entry points instead (confkv_step_begin + one "
                         "confkv_step_layer per layer, captured once in a CUDA graph and "
                         "replayed as every step); prints its own JSON line")
+    p.add_argument("--graph", action="store_true",
+                   help="time replays of one whole step (confkv_step) captured in a CUDA "
+                        "graph; prints its own JSON line")
     return p.parse_args()
 
 
@@ -600,14 +603,14 @@ def run_step_bytes(args):
     return 0
 
 
-def run_per_layer(args):
-    """Per-layer stepping: each step is confkv_step_begin (confidence and the
-    selection of every layer) followed by confkv_step_layer for every layer
-    (the new token's K/V store and that layer's attention), as a model that
-    produces each layer's query after the previous layer's attention calls it.
-    One such step is captured in a CUDA graph and replayed as every step, the
+def run_graph(args, per_layer):
+    """A step captured once in a CUDA graph and replayed as every step, the
     step's inputs copied (device to device) into the captured buffers first;
-    both are inside the timed region."""
+    both are inside the timed region.  per_layer: the step is
+    confkv_step_begin (confidence and the selection of every layer) followed
+    by confkv_step_layer for every layer (the new token's K/V store and that
+    layer's attention), as a model that produces each layer's query after the
+    previous layer's attention calls it; else one confkv_step."""
     import torch
 
     import __graft_entry__
@@ -643,6 +646,9 @@ def run_per_layer(args):
             dst.copy_(src)
 
     def one(stream=None):
+        if not per_layer:
+            kv.step(lg, q, k, v, out, kp, kc, stream=stream)
+            return
         kv.step_begin(lg, stream=stream)
         for l in range(w.L):
             kv.step_layer(l, q[l], k[l], v[l], out[l], kp[l], kc[l], stream=stream)
@@ -670,15 +676,17 @@ def run_per_layer(args):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / K
     st, rc = kv.stats()
-    line = {"metric": "decode tokens/s on 1 GB300 (full CONF-KV step, per-layer entry points)",
+    line = {"metric": "decode tokens/s on 1 GB300 (full CONF-KV step, %s)"
+                      % ("per-layer entry points" if per_layer else "CUDA-graph replays"),
             "value": w.B / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K,
             "warmup": Wm, "ms_per_step": ms, "higher_is_better": True,
             "config": {"workload": w.name, "layers": w.L, "batch": w.B,
                        "attn_splits_per_layer": "automatic",
                        "attention": kv.attention_path()},
-            "note": "confkv_step_begin + %d x confkv_step_layer per step, one CUDA graph "
-                    "replayed per step after a device-to-device copy of the step's inputs "
-                    "into the captured buffers (both timed)" % w.L,
+            "note": ("confkv_step_begin + %d x confkv_step_layer per step" % w.L
+                     if per_layer else "one confkv_step per step") +
+                    ", one CUDA graph replayed per step after a device-to-device copy of the "
+                    "step's inputs into the captured buffers (both timed)",
             "steps_on_device": st["steps"], "status": rc}
     print(json.dumps(line), flush=True)
     kv.close()
@@ -691,8 +699,8 @@ def main():
         return run_reference(args)
     if args.step_bytes:
         return run_step_bytes(args)
-    if args.per_layer:
-        return run_per_layer(args)
+    if args.per_layer or args.graph:
+        return run_graph(args, per_layer=args.per_layer)
     return run_ours(args)
 
 
