@@ -93,3 +93,26 @@ def test_step_host_optional_outputs_null():
         assert np.array_equal(ob.view(np.uint32), oa.cpu().numpy().view(np.uint32))
     a.close()
     b.close()
+
+
+@pytest.mark.parametrize("policy", [1, 2, 3])
+def test_step_host_policies(policy):
+    # WINDOW runs without logits (NULL) and writes no c / budget; H2O and
+    # RANDOM as CONF-KV: the host path equals the device step bit for bit
+    w = wl.Workload(name="host", L=2, B=2, Hq=8, Hkv=2, d=128, V=200, prefill=50, steps=8,
+                    N_high=24, N_low=40, P=4, W=12)
+    a = _prefilled(w, policy=policy, seed=5)
+    b = _prefilled(w, policy=policy, seed=5)
+    for s in range(w.steps):
+        lg, q, k, v = (np.ascontiguousarray(x) for x in wl.step_inputs(w, s))
+        oa = torch.zeros(w.L, w.B, w.Hq, w.d, device=DEV)
+        kca = torch.zeros(w.L, w.B, dtype=torch.int32, device=DEV)
+        dl = None if policy == 1 else torch.from_numpy(lg).to(DEV)
+        a.step(dl, *(torch.from_numpy(x).to(DEV) for x in (q, k, v)), oa, None, kca)
+        ob = _pinned((w.L, w.B, w.Hq, w.d), torch.float32)
+        kcb = _pinned((w.L, w.B), torch.int32)
+        b.step_host(None if policy == 1 else lg, q, k, v, ob, None, kcb)
+        assert np.array_equal(ob.view(np.uint32), oa.cpu().numpy().view(np.uint32))
+        assert np.array_equal(kcb, kca.cpu().numpy())
+    a.close()
+    b.close()
