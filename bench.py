@@ -449,6 +449,7 @@ def run_ours(args):
     prof = kv.profile_read()
     kv.profile(())
     st1, rc = kv.stats()
+    needles = needle_retention(w, kp, kc)
     # per-kernel breakdown: a separate pass of further decode steps with every
     # kernel bracketed by events (kept out of the timed region above)
     breakdown = {}
@@ -555,6 +556,7 @@ def run_ours(args):
                          "achieved_gbs": pipe, "frac": pipe / hbm,
                          "attention_share_of_step": attn_ms / ms},
             "budget_high_fraction": hi_frac,
+            **({"needle_retention": needles} if needles else {}),
             "mean_cached_tokens_per_lane": st1["cache_tokens"] / (w.L * w.B),
             "kernels_us": breakdown,
             "cpu_baseline": cpu,
@@ -569,6 +571,26 @@ def run_ours(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def needle_retention(w, kp, kc):
+    """Workloads with needle keys: how many needle positions every (layer,
+    sequence) cache still holds after the last timed step (an observable of
+    the eviction policy, not a gate)."""
+    if not w.needles:
+        return None
+    from synth import gen
+    kp_h, kc_h = kp.cpu().numpy(), kc.cpu().numpy()
+    kept = total = 0
+    for b in range(w.B):
+        pos = set(int(p) for p in gen.needle_positions(w.seed, b, w.prefill, w.W, w.needles))
+        for l in range(w.L):
+            lane = set(kp_h[l, b, :kc_h[l, b]].tolist())
+            kept += len(pos & lane)
+            total += len(pos)
+    return {"retained": kept, "total": total, "fraction": kept / total,
+            "note": "needle positions still cached after the last timed step, summed over "
+                    "every (layer, sequence)"}
 
 
 def run_step_bytes(args):
