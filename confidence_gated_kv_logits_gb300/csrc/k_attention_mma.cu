@@ -51,6 +51,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;
 constexpr int kMaxClusterSplits = 8;            // portable cluster size
+constexpr int kMaxDevicesCached = 64;           // launch-setting caches per device
 constexpr int kCorrEvery = 4;                   // INT8 chunks between V-offset corrections
 constexpr uint32_t kMagic = 0x64646464u;    // fp16 exponent byte of 1024
 constexpr uint32_t kH1152 = 0x64806480u;    // half2(1152, 1152)
@@ -945,12 +946,17 @@ __global__ void k_selftest_wait(unsigned long long limit_ns, int* gave_up, unsig
 template <int D, bool TMA>
 cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm, cudaStream_t s) {
   const int smem = kWarps * kStages * (TMA ? kTmaStage<D> : Geo<D>::STAGE) + (TMA ? 1024 : 0);
-  static bool attr_set = false;
-  if (!attr_set) {
+  // per-device caches of the function attribute and of the cluster check
+  // (the same process may drive several devices; a device number past the
+  // cache bound is simply not cached)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesCached) dev = -1;
+  static bool attr_set[kMaxDevicesCached] = {};
+  if (dev < 0 || !attr_set[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(k_attn_mma<D, TMA>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (dev >= 0) attr_set[dev] = true;
   }
   AttnParams a = ap;
   a.cluster = 0;
@@ -966,7 +972,9 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
   cfg.numAttrs = 1;
   if (ap.splits >= 2 && ap.splits <= kMaxClusterSplits) {
     // the splits of a unit as one cluster, where the device can co-schedule it
-    static int ok[kMaxClusterSplits + 1] = {};      // 0 unknown, 1 yes, -1 no
+    static int ok_cache[kMaxDevicesCached][kMaxClusterSplits + 1] = {};   // 0 unknown, 1 yes, -1 no
+    int ok_local[kMaxClusterSplits + 1] = {};
+    int* ok = dev >= 0 ? ok_cache[dev] : ok_local;
     at[1].id = cudaLaunchAttributeClusterDimension;
     at[1].val.clusterDim.x = 1;
     at[1].val.clusterDim.y = ap.splits;

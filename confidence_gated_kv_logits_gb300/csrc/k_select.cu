@@ -699,13 +699,19 @@ namespace {
 
 template <int kPolicy>
 cudaError_t launch_select_p(const Cache& c, const StepParams& sp, size_t smem, cudaStream_t s) {
-  static size_t attr = 48 * 1024;
-  if (smem > attr) {
+  // the largest dynamic shared memory set so far, per device (the same
+  // process may drive several devices; devices past the bound are not cached)
+  constexpr int kMaxDevicesCached = 64;
+  static size_t attr[kMaxDevicesCached] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesCached) dev = -1;
+  const size_t have = dev >= 0 ? attr[dev] : 0;
+  if (smem > 48 * 1024 && smem > have) {
     const cudaError_t e = cudaFuncSetAttribute(k_select<kPolicy>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr = smem;
+    if (dev >= 0) attr[dev] = smem;
   }
   const cudaError_t e = launch_pdl(k_select<kPolicy>, dim3(sp.nlb), dim3(kThreads), smem, s, c, sp);
   return e != cudaSuccess ? e : cudaGetLastError();
