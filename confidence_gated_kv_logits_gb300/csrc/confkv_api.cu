@@ -84,11 +84,13 @@ struct confkv_ctx {
   int32_t* st_kc = nullptr;
   float* st_conf = nullptr;
   int32_t* st_bud = nullptr;
-  // copy stream and events of confkv_step_host (created with the staging):
-  // [0] call start, [1] selection done, [2 + g] inputs of range g on the
-  // device, [2 + kHostGroups + g] attention of range g done
+  // copy stream, second attention stream and events of confkv_step_host
+  // (created with the staging): [0] call start, [1] selection done, [2]
+  // cache ready for the attention, [3 + g] inputs of range g on the device,
+  // [3 + kHostGroups + g] attention of range g done
   cudaStream_t cp_stream = nullptr;
-  cudaEvent_t cp_ev[2 + 2 * kHostGroups] = {};
+  cudaStream_t k_stream = nullptr;
+  cudaEvent_t cp_ev[3 + 2 * kHostGroups] = {};
   bool cp_ready = false;
   std::string msg = "ok";
   alignas(64) unsigned char tmaps[confkv::kTmaMapsBytes];          // tensor maps of the TMA attention path
@@ -123,6 +125,7 @@ void free_all(confkv_ctx* c) {
   for (cudaEvent_t& e : c->cp_ev)
     if (e) { cudaEventDestroy(e); e = nullptr; }
   if (c->cp_stream) { cudaStreamDestroy(c->cp_stream); c->cp_stream = nullptr; }
+  if (c->k_stream) { cudaStreamDestroy(c->k_stream); c->k_stream = nullptr; }
   c->cp_ready = false;
   for (int k = 0; k < kProfKernels; ++k) {
     for (cudaEvent_t e : c->ev[k]) cudaEventDestroy(e);
@@ -581,25 +584,27 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
   }
   if (!c->cp_ready) {
     if (!c->cp_stream) A(cudaStreamCreateWithFlags(&c->cp_stream, cudaStreamNonBlocking));
+    if (!c->k_stream) A(cudaStreamCreateWithFlags(&c->k_stream, cudaStreamNonBlocking));
     for (cudaEvent_t& ev : c->cp_ev)
       if (!ev) A(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
     if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("copy stream: ") + cudaGetErrorString(e));
     c->cp_ready = true;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaStream_t cs = c->cp_stream;
+  cudaStream_t cs = c->cp_stream, ks = c->k_stream;
   // once copies are enqueued, no return may leave one in flight (the
   // caller's host buffers are only borrowed for the call)
   auto drain = [&](int code) {
     cudaStreamSynchronize(cs);
+    cudaStreamSynchronize(ks);
     cudaStreamSynchronize(s);
     return code;
   };
   size_t cuts[kHostGroups + 1];
   const int G = host_ranges(c, cuts);
-  cudaEvent_t ev_start = c->cp_ev[0], ev_sel = c->cp_ev[1];
-  const cudaEvent_t* ev_in = c->cp_ev + 2;
-  const cudaEvent_t* ev_out = c->cp_ev + 2 + kHostGroups;
+  cudaEvent_t ev_start = c->cp_ev[0], ev_sel = c->cp_ev[1], ev_ready = c->cp_ev[2];
+  const cudaEvent_t* ev_in = c->cp_ev + 3;
+  const cudaEvent_t* ev_out = c->cp_ev + 3 + kHostGroups;
   // the logits first (the confidence waits for them); q, k_new and v_new
   // follow range by range on the copy stream (after the work already on
   // `stream`) while the confidence and the selection run: neither reads them
@@ -648,24 +653,30 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     prof_mark(c, 2, s);
     if (e != cudaSuccess) return drain(fail(c, CONFKV_ERR_CUDA, std::string("append: ") + cudaGetErrorString(e)));
   }
-  // one attention launch per range, as soon as its inputs are on the device;
-  // its outputs go back on the copy stream while the next range computes
+  // one attention launch per range, as soon as its inputs are on the device:
+  // the first on `stream`, the second on a second stream, so that the two
+  // grids overlap (no launch-boundary tail); each range's outputs go back on
+  // the copy stream as soon as it is done
+  A(cudaEventRecord(ev_ready, s));
   for (int gi = 0; gi < G; ++gi) {
     const size_t lb0 = cuts[gi], nlb = cuts[gi + 1] - lb0;
-    A(cudaStreamWaitEvent(s, ev_in[gi], 0));
+    cudaStream_t as = gi == 0 ? s : ks;
+    if (gi > 0) A(cudaStreamWaitEvent(as, ev_ready, 0));
+    A(cudaStreamWaitEvent(as, ev_in[gi], 0));
     const StepParams f = step_params(c, static_cast<int>(lb0), static_cast<int>(nlb),
                                      c->st_k + lb0 * c->Hkv * c->d, c->st_v + lb0 * c->Hkv * c->d,
                                      nullptr, nullptr);
-    rc = run_attention_timed(c, c->st_q + lb0 * c->Hq * c->d, c->st_out + lb0 * c->Hq * c->d, s,
+    rc = run_attention_timed(c, c->st_q + lb0 * c->Hq * c->d, c->st_out + lb0 * c->Hq * c->d, as,
                              static_cast<int>(lb0), static_cast<int>(nlb), c->splits,
                              fused ? &f : nullptr);
     if (rc != CONFKV_OK) return drain(rc);
-    A(cudaEventRecord(ev_out[gi], s));
+    A(cudaEventRecord(ev_out[gi], as));
     A(cudaStreamWaitEvent(cs, ev_out[gi], 0));
     const size_t oq = lb0 * c->Hq * c->d;
     A(cudaMemcpyAsync(out + oq, c->st_out + oq, nlb * c->Hq * c->d * sizeof(float),
                       cudaMemcpyDeviceToHost, cs));
   }
+  if (G > 1) A(cudaStreamWaitEvent(s, ev_out[G - 1], 0));     // `stream` covers every range
   c->t += 1;
   c->steps += 1;
   A(cudaStreamSynchronize(cs));
