@@ -236,15 +236,17 @@ int confkv_step_layer(confkv_ctx* ctx, int layer, const uint16_t* q, const uint1
  * and copies the outputs back, then waits for both.  The copies overlap the
  * compute: logits go first on `stream`; q, k_new and v_new travel on a
  * context-owned copy stream while the confidence and the selection (which do
- * not read them) run; large steps run the attention as several launches over
- * consecutive (layer, sequence) ranges, each range's outputs copied back
- * while the next one computes.  Pinned host memory makes the copies
+ * not read them) run; large steps run the attention as two launches over
+ * consecutive (layer, sequence) ranges (the second on a second context-owned
+ * stream, so the grids overlap), the first range's outputs copied back while
+ * the second computes.  Pinned host memory makes the copies
  * asynchronous DMA; pageable memory works but is slower.  NULL optional
  * outputs are skipped.  The results equal confkv_step's bit for bit, except
  * that kept_pos entries past kept_count are unspecified here (the whole
  * staging row is copied back).  The call synchronises, so it cannot be
  * captured in a CUDA graph.  The first call allocates the staging buffers
- * (the inputs' and outputs' sizes), a copy stream and its events.
+ * (the inputs' and outputs' sizes), a copy stream, a second attention stream
+ * and their events.
  */
 int confkv_step_host(confkv_ctx* ctx, const float* logits, const uint16_t* q,
                      const uint16_t* k_new, const uint16_t* v_new, float* out,
