@@ -92,6 +92,7 @@ struct confkv_ctx {
   cudaStream_t k_stream = nullptr;
   cudaEvent_t cp_ev[3 + 2 * kHostGroups] = {};
   bool cp_ready = false;
+  bool staged = false;        // every staging buffer allocated
   std::string msg = "ok";
   alignas(64) unsigned char tmaps[confkv::kTmaMapsBytes];          // tensor maps of the TMA attention path
   bool has_tmaps = false;
@@ -570,17 +571,20 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
                nkv = LB * c->Hkv * c->d, nkp = LB * c->Ncap;
   cudaError_t e = cudaSuccess;
   auto A = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
-  if (!c->st_logits) {
-    A(dalloc(c, &c->st_logits, nlog));
-    A(dalloc(c, &c->st_q, nq));
-    A(dalloc(c, &c->st_k, nkv));
-    A(dalloc(c, &c->st_v, nkv));
-    A(dalloc(c, &c->st_out, nq));
-    A(dalloc(c, &c->st_kp, nkp));
-    A(dalloc(c, &c->st_kc, LB));
-    A(dalloc(c, &c->st_conf, c->B));
-    A(dalloc(c, &c->st_bud, c->B));
+  if (!c->staged) {
+    // each buffer once (a call after a failed allocation completes the set)
+    auto once = [&](auto** p, size_t n) { if (!*p) A(dalloc(c, p, n)); };
+    once(&c->st_logits, nlog);
+    once(&c->st_q, nq);
+    once(&c->st_k, nkv);
+    once(&c->st_v, nkv);
+    once(&c->st_out, nq);
+    once(&c->st_kp, nkp);
+    once(&c->st_kc, LB);
+    once(&c->st_conf, static_cast<size_t>(c->B));
+    once(&c->st_bud, static_cast<size_t>(c->B));
     if (e != cudaSuccess) return fail(c, e == cudaErrorMemoryAllocation ? CONFKV_ERR_OOM : CONFKV_ERR_CUDA, "staging allocation");
+    c->staged = true;
   }
   if (!c->cp_ready) {
     if (!c->cp_stream) A(cudaStreamCreateWithFlags(&c->cp_stream, cudaStreamNonBlocking));
