@@ -13,6 +13,16 @@ before it starts.  Every step reads >1 GB of KV, far more than the 129 MB L2,
 so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--per-layer | --graph | --step-bytes]
+
+The JSON line carries the device-timed value, the attention's roofline
+(algorithmic bytes over its CUDA-event time, against the measured copy peak,
+with the DRAM traffic of the committed ncu capture), `e2e` (the same metric
+through confkv_step_host with pinned host buffers, copies inside the timed
+region), the CPU oracle baseline, the full-KV and sliding-window baselines on
+the same kernels, SM clocks sampled during the timed region and the number
+of kernel launches.  --per-layer and --graph time a captured step replayed
+as every step (per-layer entry points, or one whole step).
 
 With N > 1 (torchrun) every rank runs an independent replica (the path
 shards by sequence with no exchange): weak scaling, value = all ranks'
