@@ -29,3 +29,38 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["e2e"]["value"] == d["value"]
+
+
+def test_needle_retention_counts_cached_needles():
+    import numpy as np
+    import torch
+
+    import bench
+    from synth import gen, workloads as wl
+    w = wl.ALL["qwen14b-shaped-b1-p32768"].with_(L=3)
+    Ncap = max(w.N_low, w.N_high)
+    kp = torch.full((w.L, w.B, Ncap), -1, dtype=torch.int32)
+    kc = torch.zeros(w.L, w.B, dtype=torch.int32)
+    pos = gen.needle_positions(w.seed, 0, w.prefill, w.W, w.needles)
+    # layer 0 keeps every needle, layer 1 three of them, layer 2 none
+    for l, keep in ((0, pos), (1, pos[:3]), (2, [])):
+        lane = list(keep) + [w.prefill + 5 + i for i in range(10)]
+        kp[l, 0, :len(lane)] = torch.tensor(lane, dtype=torch.int32)
+        kc[l, 0] = len(lane)
+    kp[2, 0, 20] = int(pos[0])          # past kept_count: not counted
+    r = bench.needle_retention(w, kp, kc)
+    assert r["retained"] == w.needles + 3 and r["total"] == 3 * w.needles
+    assert bench.needle_retention(wl.ALL["qwen32b-shaped-b8-p8192"], kp, kc) is None
+
+
+def test_traffic_record_needs_the_captured_source(tmp_path, monkeypatch):
+    import bench
+    rec = json.load(open(bench.TRAFFIC_FILE))
+    src = tmp_path / "k.cu"
+    src.write_text("// some other source\n")
+    monkeypatch.setattr(bench, "ATTN_SRC", str(src))
+    assert bench.attention_traffic() is None
+    monkeypatch.setattr(bench, "ATTN_SRC", os.path.join(ROOT, "confidence_gated_kv_logits_gb300",
+                                                         "csrc", "k_attention_mma.cu"))
+    t = bench.attention_traffic()
+    assert t is not None and abs(t - rec["dram_bytes_per_launch_full_size"]) < 1.0
