@@ -24,7 +24,7 @@
 // fp32 with one rounding per operation (build with -ffp-contract=off), so the
 // ranking and the codes are decided in the same precision as the kernels'.
 //
-// Readings of points the pages leave open (each is listed in the design doc):
+// Readings of points the pages leave open (the plainest reading each time):
 //   * normalised entropy: H / ln V (natural log); V >= 2
 //   * margin m = log p(1) - log p(2) = z(1) - z(2) (top two with multiplicity)
 //   * sigma = logistic function
