@@ -68,7 +68,8 @@ class Stats(ctypes.Structure):
                 ("tokens_evicted", ctypes.c_int64), ("tokens_quantized", ctypes.c_int64),
                 ("tokens_moved", ctypes.c_int64), ("cache_tokens", ctypes.c_int64),
                 ("attn_kv_bytes", ctypes.c_int64), ("logits_bytes", ctypes.c_int64),
-                ("budget_high_steps", ctypes.c_int64), ("cache_bytes", ctypes.c_double)]
+                ("budget_high_steps", ctypes.c_int64), ("cache_bytes", ctypes.c_double),
+                ("kernel_launches", ctypes.c_int64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}

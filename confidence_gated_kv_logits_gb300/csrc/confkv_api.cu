@@ -61,6 +61,7 @@ struct confkv_ctx {
   int64_t t = 0, steps = 0;   // host view: steps launched eagerly (a replayed
                               // graph advances only the device counters)
   int64_t t0 = 0;             // prefill length
+  int64_t launches = 0;       // kernels enqueued by this context
   bool prefilled = false;
   Cache cache{};
   float* conf = nullptr;
@@ -227,6 +228,7 @@ int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s, in
   ap.mass = (c->policy == CONFKV_POLICY_CONFKV || c->policy == CONFKV_POLICY_H2O) ? 1 : 0;
   const cudaError_t e = confkv::launch_attention(c->cache, ap, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("attention launch: ") + cudaGetErrorString(e));
+  c->launches += 1;
   return CONFKV_OK;
 }
 
@@ -378,6 +380,7 @@ int confkv_prefill(confkv_ctx* c, const uint16_t* k, const uint16_t* v, int T,
   cudaError_t e = confkv::launch_prefill_store(c->cache, reinterpret_cast<const __half*>(k),
                                                reinterpret_cast<const __half*>(v), T, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("prefill: ") + cudaGetErrorString(e));
+  c->launches += 1;
   if (q_last)
     return run_attention(c, reinterpret_cast<const __half*>(q_last), c->seed_out, s, 0,
                          c->L * c->B, c->splits);
@@ -411,6 +414,7 @@ int run_confidence(confkv_ctx* c, const float* logits, float* conf_out, int32_t*
       c->cache.err, c->cache.stats, c->conf_part, c->conf_ticket, s);
   prof_mark(c, 0, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("confidence: ") + cudaGetErrorString(e));
+  c->launches += 1;
   return CONFKV_OK;
 }
 
@@ -438,6 +442,7 @@ int run_select(confkv_ctx* c, const StepParams& sp, cudaStream_t s) {
   const cudaError_t e = confkv::launch_select(c->cache, sp, s);
   prof_mark(c, 1, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("select: ") + cudaGetErrorString(e));
+  c->launches += 1;
   return CONFKV_OK;
 }
 
@@ -544,6 +549,7 @@ int confkv_step_layer(confkv_ctx* c, int layer, const uint16_t* q, const uint16_
     const cudaError_t e = confkv::launch_append(c->cache, sp, s);
     prof_mark(c, 2, s);
     if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("append: ") + cudaGetErrorString(e));
+    c->launches += 1;
   }
   rc = run_attention_timed(c, q, out, s, layer * c->B, c->B, c->splits_layer, fused ? &sp : nullptr);
   if (rc != CONFKV_OK) return rc;
@@ -656,6 +662,7 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     A(confkv::launch_append(c->cache, ap, s));
     prof_mark(c, 2, s);
     if (e != cudaSuccess) return drain(fail(c, CONFKV_ERR_CUDA, std::string("append: ") + cudaGetErrorString(e)));
+    c->launches += 1;
   }
   // one attention launch per range, as soon as its inputs are on the device:
   // the first on `stream`, the second on a second stream, so that the two
@@ -724,6 +731,7 @@ int confkv_stats(confkv_ctx* c, confkv_stats_t* out) {
   }
   out->cache_tokens = tok;
   out->cache_bytes = bytes;
+  out->kernel_launches = c->launches;
   if (err & CONFKV_FLAG_TIMEOUT) return fail(c, CONFKV_ERR_DEVICE, "a device-side wait gave up");
   if (err & CONFKV_FLAG_NONFINITE) return fail(c, CONFKV_ERR_NONFINITE_LOGITS, "non-finite logits seen");
   if (err & CONFKV_FLAG_CAPACITY) return fail(c, CONFKV_ERR_CAPACITY, "cache capacity exceeded");

@@ -508,7 +508,11 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   for (int i = 0; i < kStages - 1; ++i) issue(i);
   for (int i = 0; i < cnt; ++i) {
     if constexpr (TMA) {
-      if (!mbar_wait(smem_u32(&bars[warp][i % kStages]), (i / kStages) & 1)) {
+      // every lane waits (each needs the wait's acquire of the tile), and the
+      // warp gives up as one: lanes whose own bounded wait ran out at
+      // different times must not leave the loop apart
+      const bool ok = mbar_wait(smem_u32(&bars[warp][i % kStages]), (i / kStages) & 1);
+      if (!__all_sync(0xffffffffu, ok)) {
         ok_all = false;
         fail_i = i;
         break;

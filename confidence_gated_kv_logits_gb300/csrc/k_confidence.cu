@@ -74,12 +74,14 @@ __device__ __forceinline__ ConfState shfl_xor(const ConfState& s, int o) {
 constexpr int kThreads = 512;
 constexpr int kBatch = 8;      // logits per thread in flight per batch
 
-__global__ void __launch_bounds__(kThreads)
-k_confidence(const float* __restrict__ logits, int V, int cps, float tau, int N_low, int N_high,
-             float* conf, int32_t* hi, float* conf_out, int32_t* budget_out, int32_t* err,
-             DevStats* st, ConfPart* part, unsigned int* ticket) {
-  pdl_wait();        // the logits (and the previous step) are complete
-  pdl_trigger();     // the selection may start its EMA pass meanwhile
+// The reduction both confidence kernels share.  CTA rk of the cps CTAs of
+// sequence b reduces its slice of the row to a state, stores it in part[] and
+// takes a ticket; the CTA that takes the sequence's last ticket merges every
+// slice's state (no CTA waits) and resets the ticket.  Returns true in lane 0
+// of warp 0 of that CTA only, with the merged state in *out.
+__device__ __forceinline__ bool reduce_sequence(const float* __restrict__ logits, int V, int cps,
+                                                ConfPart* part, unsigned int* ticket,
+                                                ConfState* out) {
   const int b = blockIdx.x / cps;
   const int rk = blockIdx.x - b * cps;
   const long long lo = static_cast<long long>(V) * rk / cps;
@@ -92,7 +94,7 @@ k_confidence(const float* __restrict__ logits, int V, int cps, float tau, int N_
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       const int i = base + k * kThreads + threadIdx.x;
-      x[k] = (i < Vc) ? __ldcs(z + i) : -INFINITY;      // -inf: outside the chunk
+      x[k] = (i < Vc) ? __ldcs(z + i) : -INFINITY;      // -inf: outside the slice
     }
     // top-1 / top-2 (ties count twice) and the NaN / +inf test, branch-free
     ConfState bs{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
@@ -134,8 +136,8 @@ k_confidence(const float* __restrict__ logits, int V, int cps, float tau, int N_
     }
   }
   __syncthreads();
-  if (!s_last || warp != 0) return;
-  // last CTA of sequence b: merge every CTA's state (no CTA waits)
+  if (!s_last || warp != 0) return false;
+  // last CTA of sequence b: merge every CTA's state
   __threadfence();
   s = ConfState{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
   for (int i = lane; i < cps; i += 32) {
@@ -145,27 +147,43 @@ k_confidence(const float* __restrict__ logits, int V, int cps, float tau, int N_
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s = merge(s, shfl_xor(s, o));
-  if (lane == 0) {
-    ticket[b] = 0u;
-    float c = 0.0f;
-    const bool bad = s.bad || !(s.S > 0.0f);
-    if (!bad) {
-      const float H = logf(s.S) - s.T / s.S;
-      const float Hn = H / logf(static_cast<float>(V));
-      const float m = s.m1 - s.m2;                      // +inf when one finite logit
-      const float sig = 1.0f / (1.0f + expf(-m));
-      c = 0.4f * (1.0f - Hn) + 0.3f * sig + 0.3f / s.S;
-    } else {
-      atomicOr(err, 1);
-    }
-    const int h = (!bad && c >= tau) ? 1 : 0;
-    conf[b] = c;
-    hi[b] = h;
-    if (conf_out) conf_out[b] = c;
-    if (budget_out) budget_out[b] = h ? N_high : N_low;
-    atomicAdd(&st->logits_bytes, static_cast<unsigned long long>(V) * 4ull);
-    if (h) atomicAdd(&st->hi_steps, 1ull);
-  }
+  if (lane != 0) return false;
+  ticket[b] = 0u;
+  *out = s;
+  return true;
+}
+
+// c of a merged state (0 and *bad = true for a row with a NaN / +inf logit or
+// no finite logit): H = ln S - T/S, H^ = H / ln V, m = z(1) - z(2), p(1) = 1/S.
+__device__ __forceinline__ float confidence_of(const ConfState& s, int V, bool* bad) {
+  *bad = s.bad || !(s.S > 0.0f);
+  if (*bad) return 0.0f;
+  const float H = logf(s.S) - s.T / s.S;
+  const float Hn = H / logf(static_cast<float>(V));
+  const float m = s.m1 - s.m2;                      // +inf when one finite logit
+  const float sig = 1.0f / (1.0f + expf(-m));
+  return 0.4f * (1.0f - Hn) + 0.3f * sig + 0.3f / s.S;
+}
+
+__global__ void __launch_bounds__(kThreads)
+k_confidence(const float* __restrict__ logits, int V, int cps, float tau, int N_low, int N_high,
+             float* conf, int32_t* hi, float* conf_out, int32_t* budget_out, int32_t* err,
+             DevStats* st, ConfPart* part, unsigned int* ticket) {
+  pdl_wait();        // the logits (and the previous step) are complete
+  pdl_trigger();     // the selection may start its EMA pass meanwhile
+  ConfState s;
+  if (!reduce_sequence(logits, V, cps, part, ticket, &s)) return;
+  const int b = blockIdx.x / cps;
+  bool bad;
+  const float c = confidence_of(s, V, &bad);
+  if (bad) atomicOr(err, 1);
+  const int h = (!bad && c >= tau) ? 1 : 0;
+  conf[b] = c;
+  hi[b] = h;
+  if (conf_out) conf_out[b] = c;
+  if (budget_out) budget_out[b] = h ? N_high : N_low;
+  atomicAdd(&st->logits_bytes, static_cast<unsigned long long>(V) * 4ull);
+  if (h) atomicAdd(&st->hi_steps, 1ull);
 }
 
 }  // namespace
@@ -233,84 +251,14 @@ __global__ void __launch_bounds__(kThreads)
 k_confidence_noalloc(const float* __restrict__ logits, int V, int cps, float tau, int N_low,
                      int N_high, float* conf_out, int32_t* budget_out, int32_t* flags_out,
                      ConfPart* part, unsigned int* ticket) {
+  ConfState s;
+  if (!reduce_sequence(logits, V, cps, part, ticket, &s)) return;
   const int b = blockIdx.x / cps;
-  const int rk = blockIdx.x - b * cps;
-  const long long lo = static_cast<long long>(V) * rk / cps;
-  const long long hi_ = static_cast<long long>(V) * (rk + 1) / cps;
-  const float* z = logits + static_cast<size_t>(b) * V + lo;
-  const int Vc = static_cast<int>(hi_ - lo);
-  ConfState s{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
-  for (int base = 0; base < Vc; base += kBatch * kThreads) {
-    float x[kBatch];
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int i = base + k * kThreads + threadIdx.x;
-      x[k] = (i < Vc) ? __ldcs(z + i) : -INFINITY;
-    }
-    ConfState bs{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
-    int bad = 0;
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      bad |= !(x[k] < INFINITY) && !(x[k] == -INFINITY);
-      bs.m2 = fmaxf(bs.m2, fminf(bs.m1, x[k]));
-      bs.m1 = fmaxf(bs.m1, x[k]);
-    }
-    bs.bad = bad;
-    if (bs.m1 > -INFINITY) {
-      const float ml = bs.m1 * kL2E;
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const float xc = fmaxf(x[k], -3.0e38f);
-        const float e = ex2(fmaf(xc, kL2E, -ml));
-        bs.S += e;
-        bs.T = fmaf(e, xc - bs.m1, bs.T);
-      }
-    }
-    s = merge(s, bs);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s = merge(s, shfl_xor(s, o));
-  __shared__ ConfState sh[kThreads / 32];
-  __shared__ int s_last;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) sh[warp] = s;
-  __syncthreads();
-  if (warp == 0) {
-    s = (lane < kThreads / 32) ? sh[lane] : ConfState{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s = merge(s, shfl_xor(s, o));
-    if (lane == 0) {
-      part[blockIdx.x] = ConfPart{s.m1, s.m2, s.S, s.T, s.bad};
-      __threadfence();
-      s_last = (atomicAdd(&ticket[b], 1u) == static_cast<unsigned>(cps - 1));
-    }
-  }
-  __syncthreads();
-  if (!s_last || warp != 0) return;
-  __threadfence();
-  s = ConfState{-INFINITY, -INFINITY, 0.0f, 0.0f, 0};
-  for (int i = lane; i < cps; i += 32) {
-    const ConfPart* pp = part + static_cast<size_t>(b) * cps + i;
-    ConfState q{__ldcg(&pp->m1), __ldcg(&pp->m2), __ldcg(&pp->S), __ldcg(&pp->T), __ldcg(&pp->bad)};
-    s = merge(s, q);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s = merge(s, shfl_xor(s, o));
-  if (lane == 0) {
-    ticket[b] = 0u;
-    float c = 0.0f;
-    const bool bad = s.bad || !(s.S > 0.0f);
-    if (!bad) {
-      const float H = logf(s.S) - s.T / s.S;
-      const float Hn = H / logf(static_cast<float>(V));
-      const float m = s.m1 - s.m2;
-      const float sig = 1.0f / (1.0f + expf(-m));
-      c = 0.4f * (1.0f - Hn) + 0.3f * sig + 0.3f / s.S;
-    }
-    conf_out[b] = c;
-    if (budget_out) budget_out[b] = (!bad && c >= tau) ? N_high : N_low;
-    if (flags_out) flags_out[b] = bad ? CONFKV_FLAG_NONFINITE : 0;
-  }
+  bool bad;
+  const float c = confidence_of(s, V, &bad);
+  conf_out[b] = c;
+  if (budget_out) budget_out[b] = (!bad && c >= tau) ? N_high : N_low;
+  if (flags_out) flags_out[b] = bad ? CONFKV_FLAG_NONFINITE : 0;
 }
 
 }  // namespace

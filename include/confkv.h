@@ -132,6 +132,9 @@ typedef struct confkv_stats_t {
   int64_t logits_bytes;     /* logits bytes read by the confidence reduction */
   int64_t budget_high_steps;/* (sequence, step) pairs that chose N_high */
   double cache_bytes;       /* current bytes of cached K/V + scales */
+  int64_t kernel_launches;  /* kernels this context has enqueued, counted on
+                               the host at each launch (a captured graph's
+                               replays add none) */
 } confkv_stats_t;
 
 /* Per-kernel device time, accumulated while profiling is enabled. */

@@ -115,9 +115,39 @@ int grid_for(long long n) {
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
+// Measurement helper (not an input generator): streams a buffer once with
+// 128-bit loads, four in flight per thread, and keeps the loads live through
+// a data-dependent store that never happens for real data.  bench.py times
+// it to report the achievable HBM read rate beside the copy peak.
+__global__ void __launch_bounds__(256) k_read_probe(const int4* __restrict__ p, long long n16,
+                                                    unsigned* sink) {
+  unsigned acc = 0u;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += 4 * stride) {
+    int4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const long long j = i + u * stride;
+      v[u] = (j < n16) ? __ldcs(p + j) : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc ^= static_cast<unsigned>(v[u].x ^ v[u].y ^ v[u].z ^ v[u].w);
+  }
+  if (acc == 0x9E3779B9u && threadIdx.x == 0) sink[blockIdx.x & 63] = acc;
+}
+
 }  // namespace
 
 extern "C" {
+
+// Reads `bytes` (a multiple of 16) from `buf` once; sink: 64 words of scratch.
+int synth_read_probe(const void* buf, long long bytes, unsigned* sink, int blocks, void* stream) {
+  if (!buf || !sink || bytes <= 0 || (bytes & 15) || blocks < 1) return -1;
+  k_read_probe<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const int4*>(buf), bytes / 16, sink);
+  return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
 
 int synth_fill_f16(void* out, long long n, unsigned long long key, long long inner,
                    long long tlen, long long pos0, int heavy, void* stream) {

@@ -39,6 +39,9 @@ def lib():
         L.synth_fill_logits.restype = ctypes.c_int
         L.synth_fill_logits.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_ulonglong,
                                         ctypes.c_double, ctypes.c_void_p]
+        L.synth_read_probe.restype = ctypes.c_int
+        L.synth_read_probe.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p,
+                                       ctypes.c_int, ctypes.c_void_p]
         _lib = L
     return _lib
 
@@ -118,3 +121,27 @@ def prefill_kv(w):
                 t = torch.from_numpy(vals).to(dev)                    # [n, Hkv, d]
                 k[l, b][:, torch.from_numpy(pos_).to(dev), :] = t.permute(1, 0, 2)
     return k, v
+
+
+def read_bandwidth_gbs(gib=4, reps=5):
+    """Best-of-`reps` HBM read rate (GB/s) of one pass over a `gib` GiB buffer
+    (CUDA events around each pass; the buffer is 30x the L2)."""
+    import torch
+    n = int(gib * (1 << 30))
+    buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+    buf.fill_(1)
+    sink = torch.zeros(64, dtype=torch.int32, device="cuda")
+    sms = torch.cuda.get_device_properties(buf.device).multi_processor_count
+    best = 0.0
+    for _ in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        rc = lib().synth_read_probe(ctypes.c_void_p(buf.data_ptr()), n,
+                                    ctypes.c_void_p(sink.data_ptr()), sms * 8, _stream())
+        e1.record()
+        torch.cuda.synchronize()
+        if rc:
+            raise RuntimeError(f"synth_read_probe failed ({rc})")
+        best = max(best, n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del buf
+    return best

@@ -56,11 +56,33 @@ def test_needle_retention_counts_cached_needles():
 def test_traffic_record_needs_the_captured_source(tmp_path, monkeypatch):
     import bench
     rec = json.load(open(bench.TRAFFIC_FILE))
+    cap = rec["captured"]
+    ratio = (cap["dram_bytes_read"] + cap["dram_bytes_write"]) / cap["alg_bytes"]
     src = tmp_path / "k.cu"
     src.write_text("// some other source\n")
     monkeypatch.setattr(bench, "ATTN_SRC", str(src))
-    assert bench.attention_traffic() is None
-    monkeypatch.setattr(bench, "ATTN_SRC", os.path.join(ROOT, "confidence_gated_kv_logits_gb300",
-                                                         "csrc", "k_attention_mma.cu"))
-    t = bench.attention_traffic()
-    assert t is not None and abs(t - rec["dram_bytes_per_launch_full_size"]) < 1.0
+    assert bench.attention_traffic(1e9) == (None, None)
+    # the record names the source it was captured on: with that source, the
+    # traffic is the captured ratio times this run's algorithmic bytes
+    import hashlib
+    src.write_text("// the captured source\n")
+    rec["kernel_sha256"] = hashlib.sha256(src.read_bytes()).hexdigest()
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    t, r = bench.attention_traffic(1e9)
+    assert abs(r - ratio) < 1e-12 and abs(t - ratio * 1e9) < 1.0
+
+
+def test_budget_and_cache_traces():
+    import torch
+
+    import bench
+    from synth import workloads as wl
+    w = wl.QWEN32B.with_(L=2, B=3)
+    KC = torch.tensor([[[5, 6, 7], [8, 9, 10]], [[1, 1, 1], [1, 1, 4]]], dtype=torch.int32)
+    BD = torch.tensor([[w.N_high, w.N_low, w.N_low], [w.N_low, w.N_low, w.N_low]],
+                      dtype=torch.int32)
+    h, c = bench.budget_and_cache_traces(w, KC, BD)
+    assert h["N_high"] == 1 and h["N_low"] == 5 and h["sequences_at_N_high_per_step"] == [1, 0]
+    assert c["min"] == [5, 1] and c["max"] == [10, 4] and c["mean"] == [7.5, 1.5]

@@ -15,11 +15,9 @@ from . import parity
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
-def _check(rep, min_frac=0.6):
-    print(rep)
-    assert rep.rc == 0, rep.rc
-    assert rep.compared >= min_frac * rep.total, rep
-    return rep
+def _check(rep):
+    """Every lane-step compared with the oracle, no near-tie divergence."""
+    return parity.check(rep)
 
 
 def test_gpt2_single_layer_all_2048_steps():

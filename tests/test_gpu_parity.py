@@ -1,9 +1,9 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
 
 Tolerances (from the method's contract): INT8 codes, budgets and kept sets
-bit-exact (kept-set near-ties within 1e-6 relative of the oracle's cut, and
-budget near-ties |c - tau| < 1e-5, are counted divergences); c within 1e-5
-absolute; attention outputs within 1e-3 max-abs.
+bit-exact (a near-tie -- the oracle's keys at the cut, or its c and tau,
+within 1e-6 relative -- is a counted divergence, and every test here requires
+none); c within 1e-5 absolute; attention outputs within 1e-3 max-abs.
 """
 import numpy as np
 import pytest
@@ -102,11 +102,9 @@ def test_confidence_nonfinite_is_flagged_not_fatal():
 # whole-step parity on small shapes (several tiles, ragged tails)
 # ---------------------------------------------------------------------------
 
-def _check(rep, min_frac=0.6):
-    print(rep)
-    assert rep.rc == 0, rep.rc
-    assert rep.compared >= min_frac * rep.total, rep
-    return rep
+def _check(rep):
+    """Every lane-step compared with the oracle, no near-tie divergence."""
+    return parity.check(rep)
 
 
 def test_gqa_d128_decode_from_empty():
@@ -182,7 +180,7 @@ def test_large_values_and_scale_extremes():
 def test_sliding_window_special_case_is_exact():
     # beta = 1 freezes the EMA: keys are pure recency, identical in both precisions
     w = small(beta=1.0, prefill=60, steps=60, V=64)
-    rep = _check(parity.run(w), min_frac=1.0)
+    rep = _check(parity.run(w))
     assert rep.kept_div == 0
 
 
@@ -195,7 +193,7 @@ def test_edge_windows_and_budgets(P, W, N_high, N_low):
 
 def test_short_context_noop():
     w = small(N_high=500, N_low=500, W=500, P=8, prefill=70, steps=40)
-    rep = _check(parity.run(w), min_frac=1.0)
+    rep = _check(parity.run(w))
     assert rep.stats["tokens_evicted"] == 0
 
 
@@ -216,10 +214,14 @@ def test_needles_q_last_seed():
 
 @pytest.mark.slow
 def test_full_size_qwen32b_sampled():
+    # the benchmark's workload over its first 160 decode steps: the budget
+    # drop right after the 8192-token prefill, steady-state EMA eviction, the
+    # temperature switch at step 64 and the one-token-per-step regrowth after
+    # each drop to N_high
     w = wl.QWEN32B
     lbs = [(0, 0), (31, 5), (63, 7)]
-    rep = _check(parity.run(w, steps=3, lbs=lbs, device_inputs=True, check_codes_every=2))
-    assert rep.stats["tokens_evicted"] > 0
+    rep = _check(parity.run(w, steps=160, lbs=lbs, device_inputs=True, check_codes_every=20))
+    assert rep.stats["tokens_evicted"] > 0 and rep.steps == 160
 
 
 # ---------------------------------------------------------------------------
@@ -239,7 +241,7 @@ def test_window_full_kv_configuration():
     # budget and FP16 window at least the context: nothing evicted, nothing
     # quantised, attention over the full FP16 cache
     w = small(L=2, B=2, prefill=100, steps=40, N_high=160, N_low=160, P=8, W=160, V=64)
-    rep = _check(parity.run(w, policy=1), min_frac=1.0)
+    rep = _check(parity.run(w, policy=1))
     assert rep.stats["tokens_evicted"] == 0 and rep.stats["tokens_quantized"] == 0
 
 

@@ -1,16 +1,19 @@
-"""The allocation-free confidence entry point against the context-based step.
+"""The allocation-free confidence entry point against the context-based step
+and the CPU oracle.
 
 Runs last (file name) so that a failure here leaves every other test already
 run.  Calls go through the C ABI (ctypes) on device buffers that the test
 allocates itself; the entry point must give the same c (within the 1e-5
 tolerance the parity tests use) and the same budgets as confkv_step's conf /
-budget outputs, on two calls in a row.
+budget outputs and as the oracle's confidence, on two calls in a row.
 """
 import ctypes
 
 import numpy as np
 import pytest
 import torch
+
+import oracle
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
@@ -63,6 +66,12 @@ def test_noalloc_matches_step_on_two_calls(B, V):
         assert rc == pkg.OK
         assert np.max(np.abs(c - c_ref)) < TOL_C
         assert np.array_equal(bud, b_ref) and not fl.any()
+        lg_h = lg.cpu().numpy()
+        for b in range(B):
+            c_orc = oracle.confidence(lg_h[b])[0]
+            assert abs(float(c[b]) - c_orc) < TOL_C, (b, c[b], c_orc)
+            if abs(c_orc - tau) > TOL_C:
+                assert bud[b] == oracle.budget(c_orc, tau, n_low, n_high)
     rc, c2, bud2, _ = _noalloc(lib, batches[1], tau, n_low, n_high)   # and again on the same input
     assert rc == pkg.OK and np.array_equal(c2, c) and np.array_equal(bud2, bud)
 
@@ -79,6 +88,8 @@ def test_noalloc_flags_and_limits():
     assert c[1] == 0 and c[2] == 0 and bud[1] == 64 and bud[2] == 64
     c_ref, _ = _step_conf(pkg, lg[[0]].contiguous(), 0.5, 64, 32)
     assert abs(c[0] - c_ref[0]) < TOL_C
+    assert abs(c[0] - oracle.confidence(lg[0].cpu().numpy())[0]) < TOL_C
+    assert abs(c[3] - oracle.confidence(lg[3].cpu().numpy())[0]) < TOL_C
     big = torch.zeros(1025, 4, device=DEV)                 # batch beyond the scratch limit
     cf = torch.zeros(1025, device=DEV)
     assert lib.confkv_confidence_noalloc(_ptr(big), 1025, 4, 0.5, 64, 32, _ptr(cf), None, None,
