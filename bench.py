@@ -101,7 +101,7 @@ def workload_config(w, extra=None):
     cfg = {"workload": w.name, "layers": w.L, "q_heads": w.Hq, "kv_heads": w.Hkv,
            "head_dim": w.d, "vocab": w.V, "batch": w.B, "prefill": w.prefill,
            "N_high": w.N_high, "N_low": w.N_low, "P": w.P, "W": w.W, "tau": w.tau,
-           "ema_decay": w.beta, "pyramid_min": w.pyramid_min,
+           "ema_decay": w.beta, "pyramid_min": w.pyramid_min, "int8_channel": w.int8_channel,
            "l2": "no flush: each step reads >1 GB of KV, inputs larger than L2"}
     if extra:
         cfg.update(extra)
@@ -656,6 +656,15 @@ def run_ours(args):
     if ws == 1 and not args.no_baselines:
         base = baselines(w, ms / K, args.baseline_steps, 3, dev)
 
+    # the same workload with the per-(head, channel) INT8 storage mode
+    modes = None
+    if ws == 1 and not args.no_baselines:
+        wc = w.with_(int8_channel=1, name=f"{w.name}-int8-head-channel")
+        modes = {"int8_per_head_channel": suite_entry(wc, dev, K, Wm, hbm)}
+        modes["int8_per_head_channel"]["what"] = (
+            "INT8 rows with a per-(layer, sequence, KV head, channel) power-of-two factor fixed "
+            "at prefill, times the per-token absmax scale (confkv_opts.int8_channel = 1)")
+
     suite = None
     if ws == 1 and not args.no_suite:
         suite = [suite_entry(wl.ALL[n], dev, args.suite_steps, 3, hbm) for n in SUITE]
@@ -699,6 +708,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "baselines": base,
+            "storage_modes": modes,
             "suite": suite,
             "gpu_launches": m["launches"],
             "gpu_launches_counted": "by the library at each kernel launch in the timed region",

@@ -34,7 +34,8 @@ EXPORTS = ("confkv_create", "confkv_prefill", "confkv_step", "confkv_step_host",
            "confkv_stats", "confkv_read_cache", "confkv_profile_enable",
            "confkv_profile_read", "confkv_last_error", "confkv_free",
            "confkv_confidence_noalloc", "confkv_step_begin", "confkv_step_layer",
-           "confkv_attention_path", "confkv_selftest_bounded_wait")
+           "confkv_attention_path", "confkv_selftest_bounded_wait",
+           "confkv_read_channel_exponents")
 
 
 def selftest_bounded_wait(device=0, timeout_us=1000):
@@ -59,7 +60,7 @@ class Opts(ctypes.Structure):
                 ("max_context", ctypes.c_int), ("pyramid_min", ctypes.c_float),
                 ("device", ctypes.c_int), ("attn_splits", ctypes.c_int),
                 ("attn_kernel", ctypes.c_int), ("attn_tma", ctypes.c_int),
-                ("policy", ctypes.c_int), ("reserved", ctypes.c_int), ("seed", ctypes.c_uint64)]
+                ("policy", ctypes.c_int), ("int8_channel", ctypes.c_int), ("seed", ctypes.c_uint64)]
 
 
 class Stats(ctypes.Structure):
@@ -122,6 +123,8 @@ def load_library(path=LIB_PATH):
     L.confkv_selftest_bounded_wait.argtypes = [ci, ci, ctypes.POINTER(ci), ctypes.POINTER(ctypes.c_double)]
     L.confkv_attention_path.restype = ci
     L.confkv_attention_path.argtypes = [vp]
+    L.confkv_read_channel_exponents.restype = ci
+    L.confkv_read_channel_exponents.argtypes = [vp, ci, ci, vp, vp]
     L.confkv_confidence_noalloc.restype = ci
     L.confkv_confidence_noalloc.argtypes = [vp, ci, ci, cf, ci, ci, vp, vp, vp, vp]
     _lib = L
@@ -154,13 +157,14 @@ class ConfKV:
 
     def __init__(self, layers, heads, kv_heads, head_dim, N_low, N_high, tau, P, W,
                  ema_decay, *, batch=1, vocab, max_context=0, pyramid_min=1.0,
-                 device=None, attn_splits=0, attn_kernel=0, attn_tma=0, policy=0, seed=0):
+                 device=None, attn_splits=0, attn_kernel=0, attn_tma=0, policy=0, seed=0,
+                 int8_channel=0):
         import torch
         self._L = load_library()
         dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         self.device = dev
         opts = Opts(batch, vocab, max_context, pyramid_min, dev.index, attn_splits, attn_kernel,
-                    attn_tma, policy, 0, seed)
+                    attn_tma, policy, int8_channel, seed)
         self.policy = policy
         h = ctypes.c_void_p()
         rc = self._L.confkv_create(layers, heads, kv_heads, head_dim, N_low, N_high, tau, P,
@@ -175,6 +179,7 @@ class ConfKV:
 
     @classmethod
     def for_workload(cls, w, **kw):
+        kw.setdefault("int8_channel", getattr(w, "int8_channel", 0))
         return cls(w.L, w.Hq, w.Hkv, w.d, w.N_low, w.N_high, w.tau, w.P, w.W, w.beta,
                    batch=w.B, vocab=w.V, max_context=w.prefill, pyramid_min=w.pyramid_min,
                    **kw)
@@ -294,6 +299,15 @@ class ConfKV:
             *[ptr(r[x]) for x in ("pos", "ema", "k8", "v8", "ks", "vs", "k16", "v16", "mass")]))
         r["n8"], r["n16"] = a, c
         return r
+
+    def read_channel_exponents(self, l, b):
+        """Channel exponents (fk, fv) of (l, b): int8 [Hkv, d] each."""
+        import numpy as np
+        fk = np.zeros((self.Hkv, self.d), np.int8)
+        fv = np.zeros((self.Hkv, self.d), np.int8)
+        self._check(self._L.confkv_read_channel_exponents(
+            self._h, l, b, fk.ctypes.data_as(ctypes.c_void_p), fv.ctypes.data_as(ctypes.c_void_p)))
+        return fk, fv
 
     KERNELS = ("confidence", "select", "append", "attention")
 

@@ -57,6 +57,7 @@ struct confkv_ctx {
   std::vector<unsigned char> layer_done;
   float tau = 0.f, beta = 0.f, omb = 0.f, pyramid_min = 1.f;
   int policy = CONFKV_POLICY_CONFKV;
+  int int8_channel = 0;       // per-(head, channel) power-of-two factors on INT8 rows
   uint64_t seed = 0;
   int64_t t = 0, steps = 0;   // host view: steps launched eagerly (a replayed
                               // graph advances only the device counters)
@@ -252,7 +253,7 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
       !(pmin > 0.0f && pmin <= 1.0f) || o.attn_splits < 0 || o.attn_splits > 64 ||
       o.attn_kernel < 0 || o.attn_kernel > 2 || o.attn_tma < -1 || o.attn_tma > 0 ||
       (o.attn_kernel == 2 && heads / kv_heads > 8) || o.policy < CONFKV_POLICY_CONFKV ||
-      o.policy > CONFKV_POLICY_RANDOM || o.reserved != 0)
+      o.policy > CONFKV_POLICY_RANDOM || o.int8_channel < 0 || o.int8_channel > 1)
     return CONFKV_ERR_INVALID_ARG;
   int dev = o.device;
   if (!opts || dev < 0) cudaGetDevice(&dev);
@@ -284,6 +285,7 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   }
   c->attn_kernel = o.attn_kernel;
   c->policy = o.policy;
+  c->int8_channel = o.int8_channel;
   c->seed = o.seed;
   c->Ncap = std::max(N_low, N_high);
   // INT8 slots: the prefill's tokens older than W, and the kept tokens older
@@ -327,6 +329,8 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   A(dalloc(c, &k.n16, LB));
   A(dalloc(c, &k.new_slot, LB));
   A(dalloc(c, &k.tstep, LB));
+  k.chexp = nullptr;
+  if (c->int8_channel) A(dalloc(c, &k.chexp, U * 2 * c->d));    // zero: every factor 1
   A(dalloc(c, &k.stats, 1));
   A(dalloc(c, &k.err, 1));
   A(dalloc(c, &c->conf, c->B));
@@ -369,16 +373,25 @@ int confkv_prefill(confkv_ctx* c, const uint16_t* k, const uint16_t* v, int T,
   if (T < 0) return fail(c, CONFKV_ERR_INVALID_ARG, "T < 0");
   if (T > c->max_context) return fail(c, CONFKV_ERR_CAPACITY, "T exceeds max_context");
   if (T > 0 && (!k || !v)) return fail(c, CONFKV_ERR_INVALID_ARG, "null k or v");
-  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 1u)
-    return fail(c, CONFKV_ERR_INVALID_ARG, "misaligned k or v");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & (c->int8_channel ? 15u : 1u))
+    return fail(c, CONFKV_ERR_INVALID_ARG,
+                c->int8_channel ? "k and v must be 16-byte aligned" : "misaligned k or v");
   DeviceGuard guard(c->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   c->prefilled = true;
   c->t = T;
   c->t0 = T;
   if (T == 0) return CONFKV_OK;
-  cudaError_t e = confkv::launch_prefill_store(c->cache, reinterpret_cast<const __half*>(k),
-                                               reinterpret_cast<const __half*>(v), T, s);
+  cudaError_t e = cudaSuccess;
+  if (c->int8_channel) {
+    // the channel factors first: the store quantises with them
+    e = confkv::launch_prefill_exponents(c->cache, reinterpret_cast<const __half*>(k),
+                                         reinterpret_cast<const __half*>(v), T, s);
+    if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("prefill exponents: ") + cudaGetErrorString(e));
+    c->launches += 1;
+  }
+  e = confkv::launch_prefill_store(c->cache, reinterpret_cast<const __half*>(k),
+                                   reinterpret_cast<const __half*>(v), T, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("prefill: ") + cudaGetErrorString(e));
   c->launches += 1;
   if (q_last)
@@ -804,6 +817,29 @@ int confkv_read_cache(confkv_ctx* c, int l, int b, int cap, int* n8o, int* n16o,
     for (int i = 0; i < r8 + r16; ++i) mass[i] /= static_cast<float>(c->Hq);
   }
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, cudaGetErrorString(e));
+  return CONFKV_OK;
+}
+
+int confkv_read_channel_exponents(confkv_ctx* c, int l, int b, int8_t* k_exp, int8_t* v_exp) {
+  if (!c || l < 0 || l >= c->L || b < 0 || b >= c->B)
+    return fail(c, CONFKV_ERR_INVALID_ARG, "bad (l, b)");
+  const size_t row = static_cast<size_t>(c->d);
+  const size_t lb = static_cast<size_t>(l) * c->B + b;
+  if (!c->cache.chexp) {
+    if (k_exp) std::memset(k_exp, 0, c->Hkv * row);
+    if (v_exp) std::memset(v_exp, 0, c->Hkv * row);
+    return CONFKV_OK;
+  }
+  DeviceGuard guard(c->device);
+  std::vector<int8_t> t(static_cast<size_t>(c->Hkv) * 2 * row);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess)
+    e = cudaMemcpy(t.data(), c->cache.chexp + lb * c->Hkv * 2 * row, t.size(), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, cudaGetErrorString(e));
+  for (int h = 0; h < c->Hkv; ++h) {
+    if (k_exp) std::memcpy(k_exp + h * row, t.data() + (2 * h) * row, row);
+    if (v_exp) std::memcpy(v_exp + h * row, t.data() + (2 * h + 1) * row, row);
+  }
   return CONFKV_OK;
 }
 

@@ -7,6 +7,9 @@
 //   FP16 region   k16,v16 fp16  [L*B][Hkv][Wr][d]      (slots 0..n16-1 live;
 //                 Wr = W rounded up to 16, so whole 16-token chunks stay in bounds)
 //   metadata      pos8, ema8 [L*B][cap8]; pos16, ema16 [L*B][Wr]   (cap8 % 32 == 0)
+//   chexp         int8 [L*B][Hkv][2][d]    channel exponents f_c of K, then V
+//                 (per-(head, channel) storage mode only; else null): an INT8
+//                 element reads as code * scale * 2^f_c
 //   mass          fp32 [L*B][Hkv][slots]   attention mass of the last
 //                 attention summed over the query heads of one KV head;
 //                 slot id = INT8 slot, or cap8 + FP16 slot; slots = cap8 + Wr
@@ -105,6 +108,7 @@ struct Cache {
                       // that a captured step can be replayed)
   int32_t* new_slot;  // [L*B] FP16 slot reserved for the arriving token when the
                       // selection runs ahead of the layer's K/V (per-layer steps)
+  int8_t* chexp;      // [L*B*Hkv][2][d] channel exponents, or null (per-token scales only)
   DevStats* stats;
   int32_t* err;
 };
@@ -162,6 +166,20 @@ cudaError_t launch_select(const Cache& c, const StepParams& sp, cudaStream_t s);
 cudaError_t launch_append(const Cache& c, const StepParams& sp, cudaStream_t s);
 cudaError_t launch_prefill_store(const Cache& c, const __half* k, const __half* v, int T,
                                  cudaStream_t s);
+// Channel exponents of every (unit, K or V) from the prompt's T rows (before
+// launch_prefill_store; c.chexp must be set).
+cudaError_t launch_prefill_exponents(const Cache& c, const __half* k, const __half* v, int T,
+                                     cudaStream_t s);
+
+// 2^-f as a float for a channel exponent f in [-8, 0] (exact): the factor a
+// value is divided by before the absmax quantiser.
+__device__ __forceinline__ float chan_inv_factor(int f) {
+  return __uint_as_float(static_cast<uint32_t>(127 - f) << 23);
+}
+// 2^f as a float (f in [-8, 0]): the factor a dequantised value is multiplied by.
+__device__ __forceinline__ float chan_factor(int f) {
+  return __uint_as_float(static_cast<uint32_t>(127 + f) << 23);
+}
 cudaError_t launch_attention(const Cache& c, const AttnParams& ap, cudaStream_t s);
 // true if launch_attention runs the tensor-core kernel for this cache and
 // AttnParams::kernel (only that kernel handles AttnParams::k_new)

@@ -18,6 +18,11 @@
 // The raw scores s_{h,i} are written to `scores`; once the final (max, sum)
 // of every head is known the finishing CTA turns them into the per-token mass
 // sum_h exp(s_{h,i} - max_h) / sum_h, summed over the group.
+//
+// Per-(head, channel) storage mode (c.chexp set): an INT8 element reads as
+// code * s * 2^f_c; the INT8 keys meet a copy of the query whose channel c is
+// multiplied by 2^f_c (fp32, exact), and the INT8 values are multiplied by
+// 2^f_c as they are dequantised.
 #include <cfloat>
 
 #include "confkv_internal.cuh"
@@ -55,13 +60,22 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
 
   extern __shared__ float smem[];
   float* qs = smem;                         // [g][D]
-  float* wm = qs + g * D;                   // [kWarps][g]
+  float* qs8 = qs + g * D;                  // [g][D] query of the INT8 keys (channel factors)
+  float* wm = c.chexp ? qs8 + g * D : qs8;  // [kWarps][g]
   float* wl = wm + kWarps * g;              // [kWarps][g]
   float* fin = wl + kWarps * g;             // [2][g] final max, sum
   float* wacc = fin + 2 * g;                // [kWarps][g][D]
 
   const size_t qbase = (static_cast<size_t>(lbu) * c.Hq + kvh * g) * D;
-  for (int i = tid; i < g * D; i += kThreads) qs[i] = __half2float(ap.q[qbase + i]);
+  const int8_t* fk = c.chexp ? c.chexp + static_cast<size_t>(unit) * 2 * D : nullptr;
+  for (int i = tid; i < g * D; i += kThreads) {
+    qs[i] = __half2float(ap.q[qbase + i]);
+    if (fk) qs8[i] = qs[i] * chan_factor(fk[i % D]);
+  }
+  const float* qk8 = fk ? qs8 : qs;
+  float vfac[DPL];                           // V channel factors of this lane's channels
+#pragma unroll
+  for (int k = 0; k < DPL; ++k) vfac[k] = fk ? chan_factor(fk[D + lane + 32 * k]) : 1.0f;
   __syncthreads();
 
   float m[kMaxGroup], lsum[kMaxGroup], acc[kMaxGroup][DPL];
@@ -101,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
             const float x = static_cast<float>(static_cast<int>((ws[e >> 2] >> (8 * (e & 3))) & 0xff) - 128);
 #pragma unroll
             for (int h = 0; h < kMaxGroup; ++h)
-              if (h < g) s[h] = fmaf(x, qs[h * D + ch * 16 + e], s[h]);
+              if (h < g) s[h] = fmaf(x, qk8[h * D + ch * 16 + e], s[h]);
           }
         }
         const float sc = KS[j] * ap.scale;
@@ -155,7 +169,8 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
         const int8_t* vr = V8 + static_cast<size_t>(uu) * D;
 #pragma unroll
         for (int k = 0; k < DPL; ++k)
-          v[k] = static_cast<float>(static_cast<int>(static_cast<uint8_t>(vr[lane + 32 * k])) - 128) * vsc;
+          v[k] = static_cast<float>(static_cast<int>(static_cast<uint8_t>(vr[lane + 32 * k])) - 128) * vsc *
+                 vfac[k];
       } else {
         const __half* vr = V16 + static_cast<size_t>(uu - n8) * D;
 #pragma unroll
@@ -249,7 +264,14 @@ __global__ void __launch_bounds__(kThreads) k_attn_simple(Cache c, AttnParams ap
 
 template <int D>
 cudaError_t launch_simple(const Cache& c, const AttnParams& ap, cudaStream_t s) {
-  const size_t smem = sizeof(float) * (c.g * D + 2 * kWarps * c.g + 2 * c.g + kWarps * c.g * D);
+  const size_t smem = sizeof(float) * ((c.chexp ? 2 : 1) * c.g * D + 2 * kWarps * c.g + 2 * c.g +
+                                       kWarps * c.g * D);
+  if (smem > 48 * 1024) {          // above the default dynamic shared-memory limit
+    const cudaError_t e = cudaFuncSetAttribute(k_attn_simple<D>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
   k_attn_simple<D><<<dim3(ap.nlb * c.Hkv, ap.splits), kThreads, smem, s>>>(c, ap);
   return cudaGetLastError();
 }

@@ -30,6 +30,13 @@
 // layout (conflict-free, no cross-lane data except the 64 scales of an INT8
 // chunk).
 //
+// Per-(head, channel) storage mode (CH): an INT8 element reads as
+// code * s * 2^f_c.  For K the channel factors go into the query (q_c 2^f_c,
+// exact in fp16 for |q_c| >= 2^-6), used for the INT8 chunks; for V the
+// accumulator's channel c is multiplied by 2^f_c once, when a warp passes
+// from its INT8 chunks to its FP16 chunks (after the V offset is removed),
+// and the raw query is loaded again for the FP16 chunks.
+//
 // Split-K: with 2..8 splits the splits of a unit form one thread-block
 // cluster and merge through distributed shared memory: after a cluster
 // barrier every CTA reads the others' (max, sum) per head, computes its share
@@ -330,7 +337,7 @@ struct SoftState {
 template <int D, bool TMA>
 constexpr int kCtasPerSm = (D == 64) ? 4 : 3;
 
-template <int D, bool TMA>
+template <int D, bool TMA, bool CH>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm<D, TMA>)
 k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   using G = Geo<D>;
@@ -348,24 +355,49 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, t4 = lane & 3;
   // Q^T operand: query gid, channels t4*KPT + 4kk + {0,1} and {2,3}
   uint32_t qb[G::KS][2];
-  if (gid < g) {
-    const uint4* qp = reinterpret_cast<const uint4*>(
-        ap.q + (static_cast<size_t>(lbu) * c.Hq + kvh * g + gid) * D + t4 * G::KPT);
+  auto load_q = [&]() {
+    if (gid < g) {
+      const uint4* qp = reinterpret_cast<const uint4*>(
+          ap.q + (static_cast<size_t>(lbu) * c.Hq + kvh * g + gid) * D + t4 * G::KPT);
 #pragma unroll
-    for (int j = 0; j < G::KS / 2; ++j) {
-      const uint4 v = qp[j];
-      qb[2 * j][0] = v.x;
-      qb[2 * j][1] = v.y;
-      qb[2 * j + 1][0] = v.z;
-      qb[2 * j + 1][1] = v.w;
+      for (int j = 0; j < G::KS / 2; ++j) {
+        const uint4 v = qp[j];
+        qb[2 * j][0] = v.x;
+        qb[2 * j][1] = v.y;
+        qb[2 * j + 1][0] = v.z;
+        qb[2 * j + 1][1] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < G::KS; ++kk) qb[kk][0] = qb[kk][1] = 0u;
     }
-  } else {
-#pragma unroll
-    for (int kk = 0; kk < G::KS; ++kk) qb[kk][0] = qb[kk][1] = 0u;
-  }
+  };
+  load_q();
 
   // everything below reads the selection kernel's results
   pdl_wait();
+  if constexpr (CH) {
+    // the INT8 chunks' query: channel c times 2^f_c of this KV head's K
+    const int8_t* fk = c.chexp + static_cast<size_t>(unit) * 2 * D + t4 * G::KPT;
+#pragma unroll
+    for (int kk = 0; kk < G::KS; ++kk) {
+      const uint32_t e4 = *reinterpret_cast<const uint32_t*>(fk + 4 * kk);
+      uint32_t fac[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int f0 = static_cast<int8_t>((e4 >> (16 * hh)) & 0xffu);
+        const int f1 = static_cast<int8_t>((e4 >> (16 * hh + 8)) & 0xffu);
+        // fp16 2^f: exponent field f + 15 (f in [-8, 0]: normal)
+        fac[hh] = (static_cast<uint32_t>(f0 + 15) << 10) | (static_cast<uint32_t>(f1 + 15) << 26);
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        __half2 qv = *reinterpret_cast<__half2*>(&qb[kk][hh]);
+        qv = __hmul2(qv, *reinterpret_cast<const __half2*>(&fac[hh]));
+        qb[kk][hh] = *reinterpret_cast<uint32_t*>(&qv);
+      }
+    }
+  }
   const int n8 = c.n8[lb], n16 = c.n16[lb];
   const int nc8 = (n8 + 31) >> 5, nc16 = (n16 + 15) >> 4, nc = nc8 + nc16;
   const int cb = static_cast<int>(static_cast<long long>(nc) * split / ap.splits);
@@ -491,6 +523,23 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     ss.spB = 0.0f;
   };
 
+  // CH: the V channel factors, applied to the accumulator once the warp's
+  // INT8 chunks are done (channels gid * VPT + 2 mt + {0, 1})
+  bool v_scaled = false;
+  auto scale_v_channels = [&]() {
+    remove_offset();
+    const int8_t* fv = c.chexp + static_cast<size_t>(unit) * 2 * D + D + gid * G::VPT;
+#pragma unroll
+    for (int mt = 0; mt < G::KS; ++mt) {
+      const float f0 = chan_factor(fv[2 * mt]), f1 = chan_factor(fv[2 * mt + 1]);
+      O[mt][0] *= f0;
+      O[mt][1] *= f0;
+      O[mt][2] *= f1;
+      O[mt][3] *= f1;
+    }
+    v_scaled = true;
+  };
+
   // ---- main loop over this warp's chunks ----
   auto issue = [&](int i) {
     if constexpr (TMA) {
@@ -524,6 +573,12 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     issue(i + kStages - 1);
     const int ci = cb + warp + kWarps * i;
     const uint32_t st = wbase + (i % kStages) * STAGE;
+    if constexpr (CH) {
+      if (!v_scaled && ci >= nc8) {        // first FP16 chunk of this warp
+        scale_v_channels();
+        load_q();                          // the raw query for the FP16 tokens
+      }
+    }
     if (ci < nc8) {
       // ------------------------- INT8 chunk: 32 tokens -------------------------
       const uint32_t sks = st + (TMA ? 2 * kTmaTile<D> : G::DATA), svs = sks + 128;
@@ -695,6 +750,9 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     }
   }
   if constexpr (!TMA) cp_wait<0>();
+  if constexpr (CH) {
+    if (!v_scaled) scale_v_channels();     // the warp's chunks were all INT8 (or none)
+  }
   pdl_trigger();     // the next kernel in the stream may be scheduled
   if (split == 0 && kvh == 0) {
     // per-layer steps: the kept positions of this (layer, sequence), INT8
@@ -947,7 +1005,7 @@ __global__ void k_selftest_wait(unsigned long long limit_ns, int* gave_up, unsig
   *gave_up = ok ? 0 : 1;
 }
 
-template <int D, bool TMA>
+template <int D, bool TMA, bool CH>
 cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm, cudaStream_t s) {
   const int smem = kWarps * kStages * (TMA ? kTmaStage<D> : Geo<D>::STAGE) + (TMA ? 1024 : 0);
   // per-device caches of the function attribute and of the cluster check
@@ -957,7 +1015,7 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesCached) dev = -1;
   static bool attr_set[kMaxDevicesCached] = {};
   if (dev < 0 || !attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(k_attn_mma<D, TMA>,
+    const cudaError_t e = cudaFuncSetAttribute(k_attn_mma<D, TMA, CH>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0) attr_set[dev] = true;
@@ -988,7 +1046,7 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
       q.attrs = at + 1;
       q.numAttrs = 1;
       int n = 0;
-      const cudaError_t oe = cudaOccupancyMaxActiveClusters(&n, k_attn_mma<D, TMA>, &q);
+      const cudaError_t oe = cudaOccupancyMaxActiveClusters(&n, k_attn_mma<D, TMA, CH>, &q);
       ok[ap.splits] = (oe == cudaSuccess && n > 0) ? 1 : -1;
       if (oe != cudaSuccess) (void)cudaGetLastError();
     }
@@ -997,7 +1055,7 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
       cfg.numAttrs = 2;
     }
   }
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_mma<D, TMA>, c, a, tm);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_mma<D, TMA, CH>, c, a, tm);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -1061,25 +1119,23 @@ bool encode_attention_maps(const Cache& c, void* out) {
   return true;
 }
 
+template <int D, bool CH>
+cudaError_t launch_mma_staging(const Cache& c, const AttnParams& ap, cudaStream_t s) {
+  TmaMaps tm;
+  if (ap.tmaps) {
+    std::memcpy(&tm, ap.tmaps, sizeof(tm));
+    return launch_mma_d<D, true, CH>(c, ap, tm, s);
+  }
+  std::memset(&tm, 0, sizeof(tm));
+  return launch_mma_d<D, false, CH>(c, ap, tm, s);
+}
+
 cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStream_t s) {
   if (c.g < 1 || c.g > 8) return cudaErrorInvalidValue;
-  TmaMaps tm;
-  if (c.d == 64) {
-    if (ap.tmaps) {
-      std::memcpy(&tm, ap.tmaps, sizeof(tm));
-      return launch_mma_d<64, true>(c, ap, tm, s);
-    }
-    std::memset(&tm, 0, sizeof(tm));
-    return launch_mma_d<64, false>(c, ap, tm, s);
-  }
-  if (c.d == 128) {
-    if (ap.tmaps) {
-      std::memcpy(&tm, ap.tmaps, sizeof(tm));
-      return launch_mma_d<128, true>(c, ap, tm, s);
-    }
-    std::memset(&tm, 0, sizeof(tm));
-    return launch_mma_d<128, false>(c, ap, tm, s);
-  }
+  const bool ch = c.chexp != nullptr;
+  if (c.d == 64) return ch ? launch_mma_staging<64, true>(c, ap, s) : launch_mma_staging<64, false>(c, ap, s);
+  if (c.d == 128)
+    return ch ? launch_mma_staging<128, true>(c, ap, s) : launch_mma_staging<128, false>(c, ap, s);
   return cudaErrorInvalidValue;
 }
 

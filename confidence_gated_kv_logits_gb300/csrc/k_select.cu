@@ -167,14 +167,17 @@ __device__ __forceinline__ uint32_t quantize_lane(const float (&x)[4], int per, 
   return packed;
 }
 
-// warp-level INT8 absmax quantisation of one fp16 row of d elements
-__device__ void quantize_row_warp(const __half* src, int8_t* dst, float* scale_out, int d) {
+// warp-level INT8 absmax quantisation of one fp16 row of d elements; fe
+// (null: none) holds the row's channel exponents (x_c is divided by 2^f_c)
+__device__ void quantize_row_warp(const __half* src, int8_t* dst, float* scale_out, int d,
+                                  const int8_t* fe) {
   const int lane = threadIdx.x & 31;
   const int per = d / 32;                 // 2 or 4
   float x[4];
   float amax = 0.0f;
   for (int j = 0; j < per; ++j) {
     x[j] = __half2float(src[lane * per + j]);
+    if (fe) x[j] *= chan_inv_factor(fe[lane * per + j]);       // exact: x * 2^-f
     amax = fmaxf(amax, fabsf(x[j]));
   }
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -338,8 +341,15 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
       const int h = row >> 1;
       const __half* src = ((row & 1) ? c.v16 : c.k16) +
                           ((static_cast<size_t>(lb) * Hkv + h) * c.Wr + jage) * d + lane * per;
+      const int8_t* fe = (c.chexp && row < 2 * Hkv)
+                             ? c.chexp + ((static_cast<size_t>(lb) * Hkv + h) * 2 + (row & 1)) * d +
+                                   lane * per
+                             : nullptr;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) xr[rr][j] = (row < 2 * Hkv && j < per) ? __half2float(src[j]) : 0.0f;
+      for (int j = 0; j < 4; ++j) {
+        xr[rr][j] = (row < 2 * Hkv && j < per) ? __half2float(src[j]) : 0.0f;
+        if (fe && j < per) xr[rr][j] *= chan_inv_factor(fe[j]);   // exact: x * 2^-f
+      }
     }
 #pragma unroll
     for (int rr = 0; rr < kQRows; ++rr) qcode[rr] = quantize_lane(xr[rr], per, qscale[rr]);
@@ -572,7 +582,7 @@ for (int base = 0; base < ntok; base += kReg * kThreads) {
         const __half* src = (isv ? c.v16 : c.k16) + (u8 * c.Wr + jage) * d;
         int8_t* dst = (isv ? c.v8 : c.k8) + (u8 * cap8 + hage) * d;
         float* sc = (isv ? c.vs : c.ks) + u8 * cap8 + hage;
-        quantize_row_warp(src, dst, sc, d);
+        quantize_row_warp(src, dst, sc, d, c.chexp ? c.chexp + (u8 * 2 + (isv ? 1 : 0)) * d : nullptr);
       }
     }
   }

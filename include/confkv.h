@@ -16,7 +16,8 @@
  *      EMA mass + recency, keeps the best N, never evicting the newest P
  *                                                         [Tokenrangschikking]
  *   4. compacts the survivors contiguously and stores tokens older than the
- *      newest W as INT8 (absmax, per token and KV head) [Mixed-Precision Opslag,
+ *      newest W as INT8 (absmax, per token and KV head; optionally also a
+ *      power-of-two factor per KV head and channel)      [Mixed-Precision Opslag,
  *                                                          Implementatie]
  *   5. runs block-wise online-softmax decode attention with the INT8
  *      dequantisation fused into the block reads           [Implementatie]
@@ -113,7 +114,20 @@ typedef struct confkv_opts {
   int attn_tma;      /* tensor-core attention stages K/V tiles with TMA
                         (0, default) or with cp.async (-1) */
   int policy;        /* CONFKV_POLICY_* (default CONFKV) */
-  int reserved;      /* must be 0 */
+  int int8_channel;  /* INT8 storage [Mixed-Precision Opslag: "per head and
+                        channel"]: 0 (default) one absmax scale per (token, KV
+                        head, K or V); 1 adds one power-of-two factor 2^f_c per
+                        (layer, sequence, KV head, K or V, channel c), fixed by
+                        confkv_prefill from the prompt's channel maxima:
+                        E_c = ceil(log2 max_t |x_tc|),
+                        f_c = max(-8, E_c - max_c E_c), f_c = 0 for a channel
+                        that is zero in the prompt and for every channel when
+                        there is no prompt.  A row is stored as
+                        code_c = round-half-even(x_c 2^-f_c / s) with s the
+                        absmax/127 of x 2^-f, and read as code_c s 2^f_c (round
+                        trip within s 2^f_c / 2).  The factors belong to the
+                        head, so compaction moves tokens without re-quantising.
+                        Other values: CONFKV_ERR_INVALID_ARG. */
   uint64_t seed;     /* RANDOM policy: seed of the draws */
 } confkv_opts;
 
@@ -268,7 +282,9 @@ int confkv_stats(confkv_ctx* ctx, confkv_stats_t* out);
  * memory for inspection (synchronises).  Rows are in slot order: INT8 slots
  * first (n8 of them), then FP16 slots (n16).  Any pointer may be NULL.
  *   pos [n], ema [n]  (int32, fp32)
- *   k8, v8 [n8][Hkv][d] int8;  ks, vs [n8][Hkv] fp32 scales
+ *   k8, v8 [n8][Hkv][d] int8;  ks, vs [n8][Hkv] fp32 scales (an INT8 element
+ *   reads as code * scale, times 2^f_c of confkv_read_channel_exponents under
+ *   int8_channel = 1)
  *   k16, v16 [n16][Hkv][d] fp16 bits
  *   mass [n] fp32: the attention mass of the last attention (mean over the
  *   query heads), which the next step folds into the EMA
@@ -277,6 +293,16 @@ int confkv_stats(confkv_ctx* ctx, confkv_stats_t* out);
 int confkv_read_cache(confkv_ctx* ctx, int l, int b, int cap, int* n8, int* n16,
                       int32_t* pos, float* ema, int8_t* k8, int8_t* v8, float* ks,
                       float* vs, uint16_t* k16, uint16_t* v16, float* mass);
+
+/*
+ * confkv_read_channel_exponents -- copy the channel exponents f_c of one
+ * (layer l, sequence b) to host memory (synchronises) [Mixed-Precision
+ * Opslag, per head and channel]: k_exp, v_exp int8 [Hkv][d] (either may be
+ * NULL).  All zero (factor 1) under int8_channel = 0 or before a prompt.
+ * CONFKV_ERR_INVALID_ARG for a bad (l, b).
+ */
+int confkv_read_channel_exponents(confkv_ctx* ctx, int l, int b, int8_t* k_exp,
+                                  int8_t* v_exp);
 
 /*
  * Per-kernel CUDA-event timing of the step kernels (0 confidence, 1 select:

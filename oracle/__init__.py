@@ -37,7 +37,7 @@ class _Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("L", "B", "Hq", "Hkv", "d", "V", "N_low", "N_high", "P", "W")] + [
         ("tau", ctypes.c_float), ("beta", ctypes.c_float), ("pyramid_min", ctypes.c_double),
-        ("policy", ctypes.c_int), ("reserved", ctypes.c_int), ("seed", ctypes.c_uint64)]
+        ("policy", ctypes.c_int), ("int8_channel", ctypes.c_int), ("seed", ctypes.c_uint64)]
 
 POLICY_CONFKV, POLICY_WINDOW, POLICY_H2O, POLICY_RANDOM = 0, 1, 2, 3
 
@@ -60,6 +60,12 @@ def lib():
                                        ctypes.c_double, ctypes.c_int]
         L.orc_quantize.restype = None
         L.orc_quantize.argtypes = [vp, ctypes.c_int, vp, vp]
+        L.orc_quantize_ch.restype = None
+        L.orc_quantize_ch.argtypes = [vp, ctypes.c_int, vp, vp, vp]
+        L.orc_channel_exponents.restype = None
+        L.orc_channel_exponents.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp]
+        L.orc_get_exponents.restype = None
+        L.orc_get_exponents.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp]
         L.orc_ema_update.restype = ctypes.c_float
         L.orc_ema_update.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_float]
         L.orc_rank_key.restype = ctypes.c_float
@@ -134,13 +140,28 @@ def layer_budget(N, l, L, pyramid_min, P):
     return lib().orc_layer_budget(int(N), int(l), int(L), float(pyramid_min), int(P))
 
 
-def quantize(x):
-    """INT8 codes and fp32 scale of one fp16 row."""
+def quantize(x, f=None):
+    """INT8 codes and fp32 scale of one fp16 row; f: optional int8 channel
+    exponents (the row's channel c is divided by 2^f[c] first)."""
     xb = _bits16(x)
     codes = np.zeros(xb.size, dtype=np.int8)
     scale = np.zeros(1, dtype=np.float32)
-    lib().orc_quantize(_ptr(xb), xb.size, _ptr(codes), _ptr(scale))
+    if f is None:
+        lib().orc_quantize(_ptr(xb), xb.size, _ptr(codes), _ptr(scale))
+    else:
+        fb = _c(np.asarray(f).reshape(-1), np.int8)
+        assert fb.size == xb.size
+        lib().orc_quantize_ch(_ptr(xb), xb.size, _ptr(fb), _ptr(codes), _ptr(scale))
     return codes, np.float32(scale[0])
+
+
+def channel_exponents(x):
+    """int8 channel exponents f[d] of one KV head's prompt rows x [T, d] (fp16)."""
+    xb = _bits16(x)
+    T, d = (xb.shape if xb.ndim == 2 else (0, xb.shape[-1]))
+    f = np.zeros(d, dtype=np.int8)
+    lib().orc_channel_exponents(_ptr(xb), T, d, _ptr(f))
+    return f
 
 
 def ema_update(ema, a, beta):
@@ -194,12 +215,13 @@ class Oracle:
     """The CONF-KV cache manager of every (layer, sequence), step by step."""
 
     def __init__(self, L, B, Hq, Hkv, d, V, N_low, N_high, tau, P, W, beta,
-                 pyramid_min=1.0, policy=POLICY_CONFKV, seed=0):
+                 pyramid_min=1.0, policy=POLICY_CONFKV, seed=0, int8_channel=0):
         self.L, self.B, self.Hq, self.Hkv, self.d, self.V = L, B, Hq, Hkv, d, V
         self.N_low, self.N_high, self.P, self.W = N_low, N_high, P, W
         self.policy = policy
+        self.int8_channel = int8_channel
         prm = _Params(L, B, Hq, Hkv, d, V, N_low, N_high, P, W, tau, beta, pyramid_min,
-                      policy, 0, seed)
+                      policy, int8_channel, seed)
         self._h = lib().orc_create(ctypes.byref(prm))
         if not self._h:
             raise ValueError("oracle: invalid parameters")
@@ -207,7 +229,7 @@ class Oracle:
     @classmethod
     def for_workload(cls, w, policy=POLICY_CONFKV, seed=0):
         return cls(w.L, w.B, w.Hq, w.Hkv, w.d, w.V, w.N_low, w.N_high, w.tau, w.P,
-                   w.W, w.beta, w.pyramid_min, policy, seed)
+                   w.W, w.beta, w.pyramid_min, policy, seed, w.int8_channel)
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -261,6 +283,13 @@ class Oracle:
                                 ctypes.byref(bud), ctypes.byref(ev))
         return dict(key=key[:n], pos=pos[:n], prot=prot[:n].astype(bool),
                     budget=bud.value, evicted=ev.value)
+
+    def exponents(self, l, b):
+        """Channel exponents (fk, fv) of (l, b), int8 [Hkv, d] each."""
+        fk = np.zeros((self.Hkv, self.d), np.int8)
+        fv = np.zeros((self.Hkv, self.d), np.int8)
+        lib().orc_get_exponents(self._h, l, b, _ptr(fk), _ptr(fv))
+        return fk, fv
 
     def tokens(self, l, b):
         n = self.count(l, b)

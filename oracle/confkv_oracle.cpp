@@ -38,6 +38,16 @@
 //   * FP16 region = kept tokens with age < W; older kept tokens are INT8 with
 //     one absmax scale per (token, KV head, K or V) over the head's d channels,
 //     scale = amax/127, code = round-half-even(x/scale) clamped to [-127,127]
+//   * optional per-(head, channel) storage mode (int8_channel = 1): each
+//     (layer, sequence, KV head, K or V) also has one power-of-two factor
+//     2^f_c per channel, fixed at prefill from the prompt's channel maxima:
+//     E_c = ceil(log2 max_t |x_tc|), f_c = max(-8, E_c - max_c E_c) (0 for a
+//     channel that is zero throughout the prompt, and for every channel when
+//     there is no prompt).  A row is quantised as y_c = x_c * 2^-f_c (exact
+//     in fp32) with the per-token absmax scale s of y, and read back as
+//     code_c * s * 2^f_c; the round trip is within s * 2^f_c / 2 per element.
+//     The factors belong to the head, not to a token, so compaction (which
+//     moves single tokens) never re-quantises anything.
 //   * pyramid: N_l = max(P, floor(N*(1 - (1-pmin)*l/(L-1)) + 0.5))
 //   * prefill: no eviction; age >= W quantised; an optional last query seeds
 //     the attention mass, the EMA stays 0
@@ -90,8 +100,11 @@ struct Params {
   float tau, beta;
   double pyramid_min;
   int policy;
+  int int8_channel;
   uint64_t seed;
 };
+
+constexpr int kChannelExpMin = -8;   // smallest channel exponent f_c
 
 enum { kConfKV = 0, kWindow = 1, kH2O = 2, kRandom = 3 };
 
@@ -107,6 +120,8 @@ struct Tok {
 
 struct Lane {
   std::vector<Tok> toks;           // any order: attention is order-free
+  std::vector<int8_t> fexp;        // [2][Hkv][d] channel exponents of K, then V
+                                   // (all 0 unless int8_channel and a prompt)
   // diagnostics of the last selection
   std::vector<float> key;
   std::vector<int32_t> key_pos;
@@ -132,7 +147,7 @@ struct orc_params {
   float tau, beta;
   double pyramid_min;
   int policy;               // 0 CONF-KV, 1 WINDOW, 2 H2O, 3 RANDOM
-  int reserved;
+  int int8_channel;         // 1: per-(head, channel) power-of-two factors
   uint64_t seed;            // RANDOM draws
 };
 
@@ -190,22 +205,54 @@ int orc_layer_budget(int N, int l, int L, double pyramid_min, int P) {
   return std::max(P, n);
 }
 
-// [Mixed-Precision Opslag] one absmax INT8 row (fp32 arithmetic).
-void orc_quantize(const uint16_t* x, int d, int8_t* codes, float* scale) {
+// [Mixed-Precision Opslag] one absmax INT8 row (fp32 arithmetic).  f (null:
+// all 0) holds the row's channel exponents: channel c is divided by 2^f_c
+// before the absmax and the rounding (exact: f_c in [-8, 0]).
+void orc_quantize_ch(const uint16_t* x, int d, const int8_t* f, int8_t* codes, float* scale) {
+  std::vector<float> y(d);
   float amax = 0.0f;
   for (int c = 0; c < d; ++c) {
     const float v = static_cast<float>(half_to_double(x[c]));
-    amax = std::max(amax, std::fabs(v));
+    y[c] = f ? std::ldexp(v, -f[c]) : v;
+    amax = std::max(amax, std::fabs(y[c]));
   }
   const float s = amax / 127.0f;
   *scale = s;
   for (int c = 0; c < d; ++c) {
     if (s == 0.0f) { codes[c] = 0; continue; }
-    const float v = static_cast<float>(half_to_double(x[c]));
-    float r = round_half_even(v / s);
+    float r = round_half_even(y[c] / s);
     r = std::min(127.0f, std::max(-127.0f, r));
     codes[c] = static_cast<int8_t>(r);
   }
+}
+
+void orc_quantize(const uint16_t* x, int d, int8_t* codes, float* scale) {
+  orc_quantize_ch(x, d, nullptr, codes, scale);
+}
+
+// [Mixed-Precision Opslag], per head and channel: the channel exponents of
+// one KV head's K (or V) from the prompt's T rows x[T][d] (fp16 bits).
+// cmax_c = max_t |x_tc| (exact); E_c = ceil(log2 cmax_c) from the exact
+// binary exponent; f_c = max(-8, E_c - max E) over the channels with
+// cmax_c > 0, and f_c = 0 for the others.  T = 0 gives all zeros.
+void orc_channel_exponents(const uint16_t* x, int T, int d, int8_t* f) {
+  std::vector<double> cmax(d, 0.0);
+  for (int t = 0; t < T; ++t)
+    for (int c = 0; c < d; ++c)
+      cmax[c] = std::max(cmax[c], std::fabs(half_to_double(x[static_cast<size_t>(t) * d + c])));
+  std::vector<int> E(d, 0);
+  bool any = false;
+  int emax = 0;
+  for (int c = 0; c < d; ++c) {
+    if (cmax[c] == 0.0) continue;
+    int ex = 0;
+    const double fr = std::frexp(cmax[c], &ex);       // cmax = fr * 2^ex, fr in [0.5, 1)
+    E[c] = (fr == 0.5) ? ex - 1 : ex;                 // ceil(log2 cmax)
+    emax = any ? std::max(emax, E[c]) : E[c];
+    any = true;
+  }
+  for (int c = 0; c < d; ++c)
+    f[c] = static_cast<int8_t>(cmax[c] == 0.0 ? 0 : std::max(kChannelExpMin, E[c] - emax));
 }
 
 // [Tokenrangschikking] EMA update and ranking key, fp32 with single roundings.
@@ -294,12 +341,13 @@ orc_ctx* orc_create(const orc_params* prm) {
   const orc_params& q = *prm;
   if (q.L < 1 || q.B < 1 || q.Hkv < 1 || q.Hq < q.Hkv || q.Hq % q.Hkv || q.d < 1 ||
       q.V < 2 || q.P < 1 || q.W < q.P || q.N_low < q.P || q.N_high < q.P || q.policy < 0 ||
-      q.policy > 3)
+      q.policy > 3 || q.int8_channel < 0 || q.int8_channel > 1)
     return nullptr;
   orc_ctx* c = new orc_ctx();
   c->p = Params{q.L, q.B, q.Hq, q.Hkv, q.d, q.V, q.N_low, q.N_high, q.P, q.W,
-                q.tau, q.beta, q.pyramid_min, q.policy, q.seed};
+                q.tau, q.beta, q.pyramid_min, q.policy, q.int8_channel ? 1 : 0, q.seed};
   c->lanes.resize(static_cast<size_t>(q.L) * q.B);
+  for (Lane& ln : c->lanes) ln.fexp.assign(static_cast<size_t>(2) * q.Hkv * q.d, 0);
   c->active.assign(static_cast<size_t>(q.L) * q.B, 1);
   return c;
 }
@@ -312,27 +360,36 @@ void orc_set_active(orc_ctx* c, const uint8_t* act) {
 
 namespace {
 
-void quantize_tok(const Params& p, Tok& tk) {
+// the channel exponents of KV head h's K (isk) or V in a lane
+const int8_t* lane_fexp(const Params& p, const Lane& ln, int h, bool isk) {
+  return ln.fexp.data() + (static_cast<size_t>(isk ? 0 : 1) * p.Hkv + h) * p.d;
+}
+
+void quantize_tok(const Params& p, const Lane& ln, Tok& tk) {
   const int d = p.d;
   tk.k8.assign(static_cast<size_t>(p.Hkv) * d, 0);
   tk.v8.assign(static_cast<size_t>(p.Hkv) * d, 0);
   tk.ks.assign(p.Hkv, 0.0f);
   tk.vs.assign(p.Hkv, 0.0f);
   for (int h = 0; h < p.Hkv; ++h) {
-    orc_quantize(&tk.k16[static_cast<size_t>(h) * d], d, &tk.k8[static_cast<size_t>(h) * d], &tk.ks[h]);
-    orc_quantize(&tk.v16[static_cast<size_t>(h) * d], d, &tk.v8[static_cast<size_t>(h) * d], &tk.vs[h]);
+    orc_quantize_ch(&tk.k16[static_cast<size_t>(h) * d], d, lane_fexp(p, ln, h, true),
+                    &tk.k8[static_cast<size_t>(h) * d], &tk.ks[h]);
+    orc_quantize_ch(&tk.v16[static_cast<size_t>(h) * d], d, lane_fexp(p, ln, h, false),
+                    &tk.v8[static_cast<size_t>(h) * d], &tk.vs[h]);
   }
   tk.q8 = true;
   tk.k16.clear();
   tk.v16.clear();
 }
 
-// dequantised value of channel c of KV head h (K if isk)
-double deq(const Tok& tk, int h, int c, int d, bool isk) {
+// dequantised value of channel c of KV head h (K if isk): code * scale (the
+// fp32 product) times the channel factor 2^f_c (exact)
+double deq(const Params& p, const Lane& ln, const Tok& tk, int h, int c, bool isk) {
+  const int d = p.d;
   if (!tk.q8) return half_to_double((isk ? tk.k16 : tk.v16)[static_cast<size_t>(h) * d + c]);
   const int8_t code = (isk ? tk.k8 : tk.v8)[static_cast<size_t>(h) * d + c];
   const float s = (isk ? tk.ks : tk.vs)[h];
-  return static_cast<double>(static_cast<float>(code) * s);   // fp32 product
+  return std::ldexp(static_cast<double>(static_cast<float>(code) * s), lane_fexp(p, ln, h, isk)[c]);
 }
 
 // attention of all query heads of one lane; sets a_prev; out [Hq][d] (nullable)
@@ -344,8 +401,8 @@ void lane_attention(const Params& p, Lane& ln, const uint16_t* qlb, double* out)
   for (int h = 0; h < p.Hkv; ++h) {
     for (int i = 0; i < n; ++i)
       for (int c = 0; c < d; ++c) {
-        K[static_cast<size_t>(i) * d + c] = deq(ln.toks[i], h, c, d, true);
-        Vv[static_cast<size_t>(i) * d + c] = deq(ln.toks[i], h, c, d, false);
+        K[static_cast<size_t>(i) * d + c] = deq(p, ln, ln.toks[i], h, c, true);
+        Vv[static_cast<size_t>(i) * d + c] = deq(p, ln, ln.toks[i], h, c, false);
       }
     for (int j = 0; j < g; ++j) {
       const int hq = h * g + j;
@@ -371,6 +428,14 @@ int orc_prefill_lb(orc_ctx* c, int l, int b, const uint16_t* k, const uint16_t* 
   Lane& ln = c->lanes[static_cast<size_t>(l) * p.B + b];
   ln.toks.clear();
   const int d = p.d;
+  std::fill(ln.fexp.begin(), ln.fexp.end(), 0);
+  if (p.int8_channel && T > 0)
+    for (int h = 0; h < p.Hkv; ++h) {
+      orc_channel_exponents(k + static_cast<size_t>(h) * T * d, T, d,
+                            ln.fexp.data() + static_cast<size_t>(h) * d);
+      orc_channel_exponents(v + static_cast<size_t>(h) * T * d, T, d,
+                            ln.fexp.data() + (static_cast<size_t>(p.Hkv) + h) * d);
+    }
   for (int i = 0; i < T; ++i) {
     Tok tk;
     tk.pos = i;
@@ -382,7 +447,7 @@ int orc_prefill_lb(orc_ctx* c, int l, int b, const uint16_t* k, const uint16_t* 
         tk.k16[static_cast<size_t>(h) * d + x] = k[src];
         tk.v16[static_cast<size_t>(h) * d + x] = v[src];
       }
-    if ((T - 1) - i >= p.W) quantize_tok(p, tk);
+    if ((T - 1) - i >= p.W) quantize_tok(p, ln, tk);
     ln.toks.push_back(std::move(tk));
   }
   if (q_last && T > 0) lane_attention(p, ln, q_last, nullptr);
@@ -457,7 +522,7 @@ int orc_step(orc_ctx* c, const float* logits, const uint16_t* q, const uint16_t*
       ln.toks.swap(kept);
       // tokens leaving the most recent W are stored as INT8
       for (Tok& tk : ln.toks)
-        if (!tk.q8 && t - tk.pos >= p.W) quantize_tok(p, tk);
+        if (!tk.q8 && t - tk.pos >= p.W) quantize_tok(p, ln, tk);
       // attention over the kept tokens
       lane_attention(p, ln, q + lb * p.Hq * d, out ? out + lb * p.Hq * d : nullptr);
       if (kept_count) kept_count[lb] = static_cast<int32_t>(ln.toks.size());
@@ -516,6 +581,17 @@ int orc_get_tokens(const orc_ctx* c, int l, int b, int cap, int32_t* pos, uint8_
     }
   }
   return n;
+}
+
+// Channel exponents of (l, b): fk, fv [Hkv][d] (K, V).
+void orc_get_exponents(const orc_ctx* c, int l, int b, int8_t* fk, int8_t* fv) {
+  const Params& p = c->p;
+  const Lane& ln = c->lanes[static_cast<size_t>(l) * p.B + b];
+  const size_t n = static_cast<size_t>(p.Hkv) * p.d;
+  for (size_t i = 0; i < n; ++i) {
+    if (fk) fk[i] = ln.fexp[i];
+    if (fv) fv[i] = ln.fexp[n + i];
+  }
 }
 
 double orc_half_to_double(uint16_t h) { return half_to_double(h); }

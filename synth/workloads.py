@@ -43,6 +43,7 @@ class Workload:
     seed: int = 0
     temps: tuple = (0.3, 3.0)
     segment: int = 64
+    int8_channel: int = 0      # storage mode flag passed to the cache (not an input)
 
     @property
     def g(self):

@@ -79,6 +79,10 @@ def _legit_kept_divergence(keys, kept_o, kept_g):
 def compare_cache(kv, orc, l, b, rep):
     g = kv.read_cache(l, b)
     o = orc.tokens(l, b)
+    if orc.int8_channel:                     # per-(head, channel) exponents, bit-exact
+        gk, gv = kv.read_channel_exponents(l, b)
+        ok, ov = orc.exponents(l, b)
+        assert np.array_equal(gk, ok) and np.array_equal(gv, ov)
     assert sorted(g["pos"].tolist()) == sorted(o["pos"].tolist())
     oi = {int(p): i for i, p in enumerate(o["pos"])}
     for i in range(g["n8"]):
@@ -93,15 +97,38 @@ def compare_cache(kv, orc, l, b, rep):
     rep.code_checks += 1
 
 
+def channel_spread(d, seed=3):
+    """Per-channel powers of two in [2^-7, 1] (K; V uses them reversed): the
+    unequal channel magnitudes that the per-(head, channel) INT8 mode is for."""
+    rng = np.random.default_rng(seed)
+    return np.exp2(-rng.integers(0, 8, size=d)).astype(np.float32)
+
+
+def _spread_host(x, sc):
+    """fp16 x times per-channel powers of two, one rounding to fp16."""
+    return (x.astype(np.float32) * sc).astype(np.float16)
+
+
+def _spread_dev(x, sc):
+    """The same on the device: the fp16 product of x and a power of two is
+    exact in fp32, so torch's fp16 multiply rounds it once, like numpy."""
+    return x * torch.from_numpy(sc.astype(np.float16)).to(x.device)
+
+
 def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, splits=0,
-        logits_override=None, kernel=0, tma=0, per_layer=False, policy=0, seed=0):
+        logits_override=None, kernel=0, tma=0, per_layer=False, policy=0, seed=0, spread=None):
     """Run workload `w` on the GPU and in the oracle; return a Report.
 
     lbs: iterable of (l, b) the oracle simulates (default: all).
     device_inputs: generate the GPU's inputs with the device generator (large
       workloads); the oracle always uses the host generator.
     logits_override: optional fn(s, logits) -> logits applied to both sides.
+    spread: optional per-channel powers of two (length d) multiplying every
+      K (and, reversed, every V) row of the prefill and of each step, on both
+      sides identically.
     """
+    sk = None if spread is None else np.asarray(spread, np.float32)
+    sv = None if spread is None else sk[::-1].copy()
     import confidence_gated_kv_logits_gb300 as pkg
     dev = torch.device("cuda", 0)
     steps = w.steps if steps is None else steps
@@ -123,12 +150,16 @@ def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, spli
         if device_inputs:
             from synth import device as sd
             K, V = sd.prefill_kv(w)
+            if sk is not None:
+                K, V = _spread_dev(K, sk), _spread_dev(V, sv)
         else:
             K = np.zeros((w.L, w.B, w.Hkv, w.prefill, w.d), np.float16)
             V = np.zeros_like(K)
         ql = wl.q_last(w)
         for l, b in (lbs if device_inputs else all_lbs):
             k, v = wl.prefill_kv_lb(w, l, b)
+            if sk is not None:
+                k, v = _spread_host(k, sk), _spread_host(v, sv)
             if not device_inputs:
                 K[l, b], V[l, b] = k, v
             if mask[l, b]:
@@ -153,9 +184,13 @@ def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, spli
             lg, q, k, v = wl.step_inputs(w, s)
         if logits_override is not None:
             lg = logits_override(s, lg)
+        if sk is not None:
+            k, v = _spread_host(k, sk), _spread_host(v, sv)
         if device_inputs and logits_override is None:
             from synth import device as sd
             glg, gq, gk, gv = sd.step_inputs(w, s)
+            if sk is not None:
+                gk, gv = _spread_dev(gk, sk), _spread_dev(gv, sv)
         else:
             glg, gq, gk, gv = (to_dev(x, dev) for x in (lg, q, k, v))
         if per_layer:        # confkv_step_begin + one confkv_step_layer per layer, reversed

@@ -63,7 +63,7 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.confkv_create(*good, ctypes.byref(o_bad), ctypes.byref(h)) == pkg.ERR_INVALID_ARG
     o_bad = pkg.Opts(1, 1000, 0, 1.0, -1, 0, 0, 0, 4)          # unknown ranking policy
     assert lib.confkv_create(*good, ctypes.byref(o_bad), ctypes.byref(h)) == pkg.ERR_INVALID_ARG
-    o_bad = pkg.Opts(1, 1000, 0, 1.0, -1, 0, 0, 0, 1, 7)       # reserved field set
+    o_bad = pkg.Opts(1, 1000, 0, 1.0, -1, 0, 0, 0, 1, 7)       # unknown INT8 storage mode
     assert lib.confkv_create(*good, ctypes.byref(o_bad), ctypes.byref(h)) == pkg.ERR_INVALID_ARG
     assert lib.confkv_create(*good, ctypes.byref(o), None) == pkg.ERR_INVALID_ARG
     # null contexts

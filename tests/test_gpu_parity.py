@@ -265,3 +265,69 @@ def test_bounded_wait_gives_up_and_device_stays_usable():
     assert 2000.0 <= waited_us < 200000.0
     w = small(steps=6)
     _check(parity.run(w))
+
+
+# ---------------------------------------------------------------------------
+# per-(head, channel) INT8 storage (Mixed-Precision Opslag, "per head and
+# channel"): power-of-two channel factors fixed at prefill, on every kernel
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("splits", [1, 3])
+@pytest.mark.parametrize("kernel,tma", [(0, 0), (2, -1), (1, 0)])
+def test_channel_mode_parity(d, splits, kernel, tma):
+    w = small(prefill=120, steps=50, V=64, d=d, int8_channel=1)
+    rep = _check(parity.run(w, splits=splits, kernel=kernel, tma=tma,
+                            spread=parity.channel_spread(d), check_codes_every=7))
+    assert rep.code_checks > 0 and rep.stats["tokens_quantized"] > 0
+
+
+def test_channel_mode_exponents_are_nontrivial_and_fixed():
+    import confidence_gated_kv_logits_gb300 as pkg
+    w = small(prefill=64, steps=10, V=64, int8_channel=1)
+    sc = parity.channel_spread(w.d)
+    kv = pkg.ConfKV.for_workload(w, device=0)
+    K = np.zeros((w.L, w.B, w.Hkv, w.prefill, w.d), np.float16)
+    V = np.zeros_like(K)
+    for l in range(w.L):
+        for b in range(w.B):
+            k, v = wl.prefill_kv_lb(w, l, b)
+            K[l, b], V[l, b] = parity._spread_host(k, sc), parity._spread_host(v, sc[::-1].copy())
+    kv.prefill(parity.to_dev(K, DEV), parity.to_dev(V, DEV), w.prefill)
+    fk0, fv0 = kv.read_channel_exponents(1, 2)
+    want = np.stack([oracle.channel_exponents(K[1, 2, h]) for h in range(w.Hkv)])
+    assert np.array_equal(fk0, want) and len(set(fk0.ravel().tolist())) >= 4
+    out = torch.zeros(w.L, w.B, w.Hq, w.d, device=DEV)
+    for s in range(w.steps):
+        lg, q, k, v = (parity.to_dev(x, DEV) for x in wl.step_inputs(w, s))
+        kv.step(lg, q, k, v, out)
+    fk1, fv1 = kv.read_channel_exponents(1, 2)
+    assert np.array_equal(fk0, fk1) and np.array_equal(fv0, fv1)
+    kv.close()
+    # without the mode, or without a prompt, every factor is 1
+    w0 = small(prefill=0, steps=3, V=64, int8_channel=1)
+    kv = pkg.ConfKV.for_workload(w0, device=0)
+    assert not any(x.any() for x in kv.read_channel_exponents(0, 0))
+    kv.close()
+
+
+def test_channel_mode_mha_and_decode_from_empty():
+    # 12 KV heads: the selection quantises the aging token row by row (the
+    # warp-per-row path); no prompt: every factor is 1
+    _check(parity.run(wl.GPT2_L1.with_(steps=300, prefill=200, int8_channel=1),
+                      spread=parity.channel_spread(64), check_codes_every=50))
+    _check(parity.run(small(prefill=0, steps=60, V=64, int8_channel=1)))
+
+
+def test_channel_mode_per_layer_and_policies():
+    w = small(L=3, B=2, Hq=40, Hkv=8, prefill=70, steps=25, V=64, int8_channel=1)
+    _check(parity.run(w, per_layer=True, spread=parity.channel_spread(w.d)))
+    _check(parity.run(w, policy=2, spread=parity.channel_spread(w.d)))
+
+
+@pytest.mark.slow
+def test_full_size_qwen32b_channel_mode_sampled():
+    w = wl.QWEN32B.with_(int8_channel=1)
+    rep = _check(parity.run(w, steps=40, lbs=[(0, 0), (40, 3)], device_inputs=True,
+                            check_codes_every=13, spread=parity.channel_spread(w.d)))
+    assert rep.stats["tokens_evicted"] > 0
