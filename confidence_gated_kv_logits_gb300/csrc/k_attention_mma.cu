@@ -30,6 +30,12 @@
 // layout (conflict-free, no cross-lane data except the 64 scales of an INT8
 // chunk).
 //
+// With one split per unit (whole steps), each warp requests the tiles of its
+// first chunk -- an INT8 chunk whenever the unit holds enough of them --
+// before it reads the region sizes, so that the two round trips of the
+// prologue overlap.  Under per-layer stepping the kept positions of a
+// (layer, sequence) are copied by all of its CTAs, one slice each.
+//
 // Per-(head, channel) storage mode (CH): an INT8 element reads as
 // code * s * 2^f_c.  For K the channel factors go into the query (q_c 2^f_c,
 // exact in fp16 for |q_c| >= 2^-6), used for the INT8 chunks; for V the
@@ -398,12 +404,30 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       }
     }
   }
+  const uint32_t wbase = smem_u32(smem) + warp * kStages * STAGE;
+  // Speculative first tile (TMA, one split, whole steps): warp w's first
+  // chunk is chunk w, an INT8 chunk whenever the unit holds more than w INT8
+  // chunks (every unit of a long context).  Its tiles are requested before
+  // the region sizes are read, so that the two round trips overlap; a wrong
+  // guess costs one wasted tile and shifts the warp's stage sequence by one.
+  // The guard keeps the tile inside the INT8 arrays for every unit.
+  bool spec = false;
+  if constexpr (TMA) {
+    if (lane == 0)
+      for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    __syncwarp();
+    spec = ap.splits == 1 && !ap.k_new && c.cap8 >= 32 * kWarps;
+    if (spec && lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      issue_chunk_tma<D>(c, tm, unit, 0x7fffffff, warp, wbase, smem_u32(&bars[warp][0]));
+    }
+  }
   const int n8 = c.n8[lb], n16 = c.n16[lb];
   const int nc8 = (n8 + 31) >> 5, nc16 = (n16 + 15) >> 4, nc = nc8 + nc16;
   const int cb = static_cast<int>(static_cast<long long>(nc) * split / ap.splits);
   const int ce = static_cast<int>(static_cast<long long>(nc) * (split + 1) / ap.splits);
   const int cnt = (ce - cb > warp) ? (ce - cb - warp + kWarps - 1) / kWarps : 0;
-  const uint32_t wbase = smem_u32(smem) + warp * kStages * STAGE;
   // Per-layer steps: the selection ran ahead and reserved FP16 slot hn for the
   // arriving token.  The one CTA whose chunk range holds that slot stores the
   // token's K/V rows of this KV head before any of its tiles is read.
@@ -425,14 +449,22 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       if constexpr (TMA) asm volatile("fence.proxy.async.global;\n" ::: "memory");
     }
   }
-  if constexpr (TMA) {
-    if (lane == 0)
-      for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    __syncwarp();
-  }
   bool ok_all = true;
   int fail_i = 0;
+  // stage offset of the warp's chunk sequence: 1 after a wasted speculative tile
+  int so = 0;
+  const bool spec_hit = spec && cnt > 0 && cb + warp < nc8;
+  if constexpr (TMA) {
+    if (spec && !spec_hit) {
+      // the guess was wrong: the wasted tile must land before its stage is reused
+      const bool ok = mbar_wait(smem_u32(&bars[warp][0]), 0);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok_all = false;
+        fail_i = -1;
+      }
+      so = 1;
+    }
+  }
 
   float O[G::KS][4];
 #pragma unroll
@@ -545,8 +577,9 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     if constexpr (TMA) {
       if (lane == 0 && i < cnt) {
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        issue_chunk_tma<D>(c, tm, unit, nc8, cb + warp + kWarps * i, wbase + (i % kStages) * STAGE,
-                        smem_u32(&bars[warp][i % kStages]));
+        issue_chunk_tma<D>(c, tm, unit, nc8, cb + warp + kWarps * i,
+                           wbase + ((i + so) % kStages) * STAGE,
+                           smem_u32(&bars[warp][(i + so) % kStages]));
       }
     } else {
       if (i < cnt) issue_chunk<D>(c, unit, nc8, cb + warp + kWarps * i, wbase + (i % kStages) * STAGE, lane);
@@ -554,13 +587,14 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     }
   };
 #pragma unroll
-  for (int i = 0; i < kStages - 1; ++i) issue(i);
-  for (int i = 0; i < cnt; ++i) {
+  for (int i = 0; i < kStages - 1; ++i)
+    if (!(spec_hit && i == 0)) issue(i);                 // chunk 0 may be in flight already
+  for (int i = 0; i < (ok_all ? cnt : 0); ++i) {
     if constexpr (TMA) {
       // every lane waits (each needs the wait's acquire of the tile), and the
       // warp gives up as one: lanes whose own bounded wait ran out at
       // different times must not leave the loop apart
-      const bool ok = mbar_wait(smem_u32(&bars[warp][i % kStages]), (i / kStages) & 1);
+      const bool ok = mbar_wait(smem_u32(&bars[warp][(i + so) % kStages]), ((i + so) / kStages) & 1);
       if (!__all_sync(0xffffffffu, ok)) {
         ok_all = false;
         fail_i = i;
@@ -572,7 +606,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     __syncwarp();
     issue(i + kStages - 1);
     const int ci = cb + warp + kWarps * i;
-    const uint32_t st = wbase + (i % kStages) * STAGE;
+    const uint32_t st = wbase + ((i + so) % kStages) * STAGE;
     if constexpr (CH) {
       if (!v_scaled && ci >= nc8) {        // first FP16 chunk of this warp
         scale_v_channels();
@@ -754,23 +788,40 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     if (!v_scaled) scale_v_channels();     // the warp's chunks were all INT8 (or none)
   }
   pdl_trigger();     // the next kernel in the stream may be scheduled
-  if (split == 0 && kvh == 0) {
+  if (ap.kept_pos) {
     // per-layer steps: the kept positions of this (layer, sequence), INT8
-    // slots then FP16 slots
-    if (ap.kept_pos) {
-      const int32_t* pos8 = c.pos8 + static_cast<size_t>(lb) * c.cap8;
-      const int32_t* pos16 = c.pos16 + static_cast<size_t>(lb) * c.Wr;
-      int32_t* kp = ap.kept_pos + static_cast<size_t>(lbu) * c.Ncap;
-      for (int i = tid; i < n8 + n16; i += kThreads) kp[i] = (i < n8) ? pos8[i] : pos16[i - n8];
+    // slots then FP16 slots, copied by all its CTAs (one slice each, every
+    // thread's loads issued before its stores)
+    const int32_t* __restrict__ pos8 = c.pos8 + static_cast<size_t>(lb) * c.cap8;
+    const int32_t* __restrict__ pos16 = c.pos16 + static_cast<size_t>(lb) * c.Wr;
+    int32_t* __restrict__ kp = ap.kept_pos + static_cast<size_t>(lbu) * c.Ncap;
+    const int parts = ap.splits * c.Hkv, part = split * c.Hkv + kvh, n = n8 + n16;
+    const int per = (n + parts - 1) / parts;
+    const int i0 = part * per, i1 = min(n, i0 + per);
+    for (int base = i0; base < i1; base += 4 * kThreads) {
+      int v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * kThreads + tid;
+        v[u] = (i < i1) ? ((i < n8) ? pos8[i] : pos16[i - n8]) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * kThreads + tid;
+        if (i < i1) kp[i] = v[u];
+      }
     }
-    if (ap.kept_count && tid == 0) ap.kept_count[lbu] = n8 + n16;
   }
+  if (split == 0 && kvh == 0 && ap.kept_count && tid == 0) ap.kept_count[lbu] = n8 + n16;
   if (!ok_all) {
     // a tile never arrived: flag the step (its output for this unit is
     // incomplete) and give the copy in flight one more bounded wait before
     // the shared memory is reused
     if (lane == 0) atomicOr(c.err, 4);
-    mbar_wait(smem_u32(&bars[warp][fail_i % kStages]), (fail_i / kStages) & 1);
+    if (fail_i >= 0)
+      mbar_wait(smem_u32(&bars[warp][(fail_i + so) % kStages]), ((fail_i + so) / kStages) & 1);
+    else
+      mbar_wait(smem_u32(&bars[warp][0]), 0);      // the wasted speculative tile
   }
 
   // ---- merge the warps of this CTA (shared memory reused) ----
