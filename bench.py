@@ -64,6 +64,9 @@ def parse():
     p.add_argument("--no-suite", action="store_true",
                    help="skip the short runs of every other workload of the suite")
     p.add_argument("--suite-steps", type=int, default=32)
+    p.add_argument("--no-per-layer", action="store_true",
+                   help="skip the short timing of the per-layer entry points")
+    p.add_argument("--per-layer-steps", type=int, default=64)
     p.add_argument("--suite", action="store_true",
                    help="print one JSON line per workload of the suite (--steps each) instead")
     p.add_argument("--layers", type=int, default=0,
@@ -665,6 +668,17 @@ def run_ours(args):
             "INT8 rows with a per-(layer, sequence, KV head, channel) power-of-two factor fixed "
             "at prefill, times the per-token absmax scale (confkv_opts.int8_channel = 1)")
 
+    # the per-layer entry points (a model's view: begin + one launch per layer),
+    # one captured step replayed per step
+    per_layer = None
+    if ws == 1 and not args.no_per_layer:
+        import copy
+        pa = copy.copy(args)
+        pa.steps, pa.warmup = args.per_layer_steps, 3
+        r = run_graph(pa, per_layer=True, emit=False)
+        per_layer = {"ms_per_step": r["ms_per_step"], "tokens_per_s": r["value"],
+                     "steps": r["steps"], "note": r["note"], "status": r["status"]}
+
     suite = None
     if ws == 1 and not args.no_suite:
         suite = [suite_entry(wl.ALL[n], dev, args.suite_steps, 3, hbm) for n in SUITE]
@@ -709,6 +723,7 @@ def run_ours(args):
             "e2e": e2e,
             "baselines": base,
             "storage_modes": modes,
+            "per_layer": per_layer,
             "suite": suite,
             "gpu_launches": m["launches"],
             "gpu_launches_counted": "by the library at each kernel launch in the timed region",
@@ -774,7 +789,7 @@ def run_step_bytes(args):
     return 0
 
 
-def run_graph(args, per_layer):
+def run_graph(args, per_layer, emit=True):
     """A step captured once in a CUDA graph and replayed as every step, the
     step's inputs copied (device to device) into the captured buffers first;
     both are inside the timed region.  per_layer: the step is
@@ -788,8 +803,9 @@ def run_graph(args, per_layer):
     __graft_entry__.build()
     import confidence_gated_kv_logits_gb300 as pkg
     from synth import device as sd, workloads as wl
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
+    if emit:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
     w = get_workload(args)
     K, Wm = args.steps, args.warmup
     S = K + Wm + 1
@@ -859,8 +875,12 @@ def run_graph(args, per_layer):
                     ", one CUDA graph replayed per step after a device-to-device copy of the "
                     "step's inputs into the captured buffers (both timed)",
             "steps_on_device": st["steps"], "status": rc}
-    print(json.dumps(line), flush=True)
     kv.close()
+    del LG, Q, KN, VN
+    torch.cuda.empty_cache()
+    if not emit:
+        return line
+    print(json.dumps(line), flush=True)
     return 0 if rc == 0 else 1
 
 

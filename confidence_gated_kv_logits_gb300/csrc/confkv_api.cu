@@ -53,6 +53,7 @@ struct confkv_ctx {
   int sms = kSmCountDefault;   // the device's SM count (launch-shape heuristics)
   // per-layer stepping (confkv_step_begin / confkv_step_layer)
   bool step_open = false;
+  bool layered = false;       // a per-layer step has been begun: masses may be deferred
   int layers_left = 0;
   std::vector<unsigned char> layer_done;
   float tau = 0.f, beta = 0.f, omb = 0.f, pyramid_min = 1.f;
@@ -205,7 +206,7 @@ int auto_splits_layer(int units, int ncap, int d, int sms) {
 }
 
 int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s, int lb0, int nlb,
-                  int splits, const StepParams* fused = nullptr) {
+                  int splits, const StepParams* fused = nullptr, bool defer_mass = false) {
   AttnParams ap{};
   if (fused) {
     ap.k_new = fused->k_new;
@@ -225,8 +226,10 @@ int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s, in
   ap.ticket = c->ticket;
   ap.scale = 1.0f / std::sqrt(static_cast<float>(c->d));
   // the per-token attention mass feeds only the EMA (CONF-KV) and the
-  // accumulated mass (H2O)
-  ap.mass = (c->policy == CONFKV_POLICY_CONFKV || c->policy == CONFKV_POLICY_H2O) ? 1 : 0;
+  // accumulated mass (H2O); per-layer launches defer it to the next step
+  const bool uses = c->policy == CONFKV_POLICY_CONFKV || c->policy == CONFKV_POLICY_H2O;
+  ap.mass = (uses && !defer_mass) ? 1 : 0;
+  ap.defer_mass = (uses && defer_mass) ? 1 : 0;
   const cudaError_t e = confkv::launch_attention(c->cache, ap, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("attention launch: ") + cudaGetErrorString(e));
   c->launches += 1;
@@ -329,6 +332,8 @@ int confkv_create(int layers, int heads, int kv_heads, int head_dim, int N_low, 
   A(dalloc(c, &k.n16, LB));
   A(dalloc(c, &k.new_slot, LB));
   A(dalloc(c, &k.tstep, LB));
+  A(dalloc(c, &k.fin, LB * c->Hq * 2));
+  A(dalloc(c, &k.mass_pending, U));
   k.chexp = nullptr;
   if (c->int8_channel) A(dalloc(c, &k.chexp, U * 2 * c->d));    // zero: every factor 1
   A(dalloc(c, &k.stats, 1));
@@ -450,6 +455,19 @@ StepParams step_params(const confkv_ctx* c, int lb0, int nlb, const uint16_t* k_
   return sp;
 }
 
+// The masses that per-layer attention launches deferred, computed before
+// anything reads them (a no-op on the device for lanes with nothing pending).
+int run_mass_finalise(confkv_ctx* c, cudaStream_t s) {
+  const cudaError_t e = confkv::launch_mass_finalise(c->cache, s);
+  if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("mass finalise: ") + cudaGetErrorString(e));
+  c->launches += 1;
+  return CONFKV_OK;
+}
+
+bool uses_mass(const confkv_ctx* c) {
+  return c->policy == CONFKV_POLICY_CONFKV || c->policy == CONFKV_POLICY_H2O;
+}
+
 int run_select(confkv_ctx* c, const StepParams& sp, cudaStream_t s) {
   prof_mark(c, 1, s);
   const cudaError_t e = confkv::launch_select(c->cache, sp, s);
@@ -460,9 +478,11 @@ int run_select(confkv_ctx* c, const StepParams& sp, cudaStream_t s) {
 }
 
 int run_attention_timed(confkv_ctx* c, const uint16_t* q, float* out, cudaStream_t s, int lb0,
-                        int nlb, int splits, const StepParams* fused = nullptr) {
+                        int nlb, int splits, const StepParams* fused = nullptr,
+                        bool defer_mass = false) {
   prof_mark(c, 3, s);
-  const int rc = run_attention(c, reinterpret_cast<const __half*>(q), out, s, lb0, nlb, splits, fused);
+  const int rc = run_attention(c, reinterpret_cast<const __half*>(q), out, s, lb0, nlb, splits, fused,
+                               defer_mass);
   prof_mark(c, 3, s);
   return rc;
 }
@@ -505,6 +525,10 @@ int confkv_step(confkv_ctx* c, const float* logits, const uint16_t* q, const uin
   if (c->t >= 0x7fffffffLL) return fail(c, CONFKV_ERR_STATE, "position overflow");
   DeviceGuard guard(c->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c->layered && uses_mass(c)) {
+    rc = run_mass_finalise(c, s);
+    if (rc != CONFKV_OK) return rc;
+  }
   if (uses_confidence(c)) {
     rc = run_confidence(c, logits, conf_out, budget_out, s);
     if (rc != CONFKV_OK) return rc;
@@ -526,6 +550,14 @@ int confkv_step_begin(confkv_ctx* c, const float* logits, float* conf_out, int32
   if (c->t >= 0x7fffffffLL) return fail(c, CONFKV_ERR_STATE, "position overflow");
   DeviceGuard guard(c->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the previous per-layer step's layers deferred their attention mass; it is
+  // computed here, before the selection folds it into the EMA (always
+  // launched, so that a captured step does it on every replay)
+  c->layered = true;
+  if (uses_mass(c)) {
+    const int rc = run_mass_finalise(c, s);
+    if (rc != CONFKV_OK) return rc;
+  }
   if (uses_confidence(c)) {
     const int rc = run_confidence(c, logits, conf_out, budget_out, s);
     if (rc != CONFKV_OK) return rc;
@@ -564,7 +596,10 @@ int confkv_step_layer(confkv_ctx* c, int layer, const uint16_t* q, const uint16_
     if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("append: ") + cudaGetErrorString(e));
     c->launches += 1;
   }
-  rc = run_attention_timed(c, q, out, s, layer * c->B, c->B, c->splits_layer, fused ? &sp : nullptr);
+  // the tensor-core attention defers this layer's mass to the next step's
+  // first kernel, so that the layer's launch ends with its output
+  rc = run_attention_timed(c, q, out, s, layer * c->B, c->B, c->splits_layer, fused ? &sp : nullptr,
+                           fused);
   if (rc != CONFKV_OK) return rc;
   c->layer_done[layer] = 1;
   if (--c->layers_left == 0) {
@@ -644,6 +679,10 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
   }
   if (e != cudaSuccess) return drain(fail(c, CONFKV_ERR_CUDA, std::string("H2D: ") + cudaGetErrorString(e)));
   int rc;
+  if (c->layered && uses_mass(c)) {
+    rc = run_mass_finalise(c, s);
+    if (rc != CONFKV_OK) return drain(rc);
+  }
   if (uses_confidence(c)) {
     rc = run_confidence(c, c->st_logits, conf_out ? c->st_conf : nullptr,
                         budget_out ? c->st_bud : nullptr, s);
@@ -757,6 +796,10 @@ int confkv_read_cache(confkv_ctx* c, int l, int b, int cap, int* n8o, int* n16o,
   if (!c || l < 0 || l >= c->L || b < 0 || b >= c->B || cap < 0)
     return fail(c, CONFKV_ERR_INVALID_ARG, "bad (l, b) or cap");
   DeviceGuard guard(c->device);
+  if (mass && c->layered && uses_mass(c) && !c->step_open) {
+    const int rc = run_mass_finalise(c, nullptr);     // deferred masses first
+    if (rc != CONFKV_OK) return rc;
+  }
   cudaError_t e = cudaDeviceSynchronize();
   const size_t lb = static_cast<size_t>(l) * c->B + b;
   int n8 = 0, n16 = 0;

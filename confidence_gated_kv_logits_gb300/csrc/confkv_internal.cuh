@@ -14,6 +14,11 @@
 //                 attention summed over the query heads of one KV head;
 //                 slot id = INT8 slot, or cap8 + FP16 slot; slots = cap8 + Wr
 //   scores        fp32 [L*B][Hq][slots]    raw scores of the last attention
+//   fin           fp32 [L*B][Hq][2]        (max, sum) of each query head's last
+//                 attention, kept when a per-layer launch defers the mass
+//   mass_pending  int32 [L*B][Hkv]         1: the unit's mass is still to be
+//                 computed from scores and fin (deferred by per-layer launches);
+//                 cleared by the CTA that computes it, so finalising twice is a no-op
 // Both regions are dense (contiguous compaction): live slots are always
 // [0, n8) and [0, n16), so the attention streams them without any indirection.
 #pragma once
@@ -109,6 +114,8 @@ struct Cache {
   int32_t* new_slot;  // [L*B] FP16 slot reserved for the arriving token when the
                       // selection runs ahead of the layer's K/V (per-layer steps)
   int8_t* chexp;      // [L*B*Hkv][2][d] channel exponents, or null (per-token scales only)
+  float* fin;         // [L*B][Hq][2] per-head (max, sum) of a deferred mass
+  int32_t* mass_pending;  // [L*B*Hkv] the unit's mass awaits launch_mass_finalise
   DevStats* stats;
   int32_t* err;
 };
@@ -142,6 +149,8 @@ struct AttnParams {
   unsigned int* ticket;  // [L*B*Hkv]
   float scale;           // 1/sqrt(d)
   int mass;              // 1: write the per-token attention mass (EMA / H2O policies)
+  int defer_mass;        // 1: keep the raw scores and each head's (max, sum) instead
+                         // and flag the lane; launch_mass_finalise computes the mass
   int cluster;           // set by the launcher: the splits of a unit are one cluster
   // Per-layer steps on the tensor-core path (else null): the arriving token's
   // K/V [nlb][Hkv][d], stored into the FP16 slot the selection reserved
@@ -185,6 +194,10 @@ cudaError_t launch_attention(const Cache& c, const AttnParams& ap, cudaStream_t 
 // AttnParams::kernel (only that kernel handles AttnParams::k_new)
 bool attention_uses_mma(const Cache& c, int kernel);
 cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStream_t s);
+// The per-token attention mass of every lane whose attention deferred it
+// (mass_pending), from the raw scores and per-head (max, sum) the attention
+// kept, with the same arithmetic as the attention's own mass epilogue.
+cudaError_t launch_mass_finalise(const Cache& c, cudaStream_t s);
 // Encodes the four tensor maps of the TMA attention path into `out`
 // (kTmaMapsBytes bytes, 64-byte aligned); returns false if the driver cannot
 // or the cache is too large for 32-bit tile coordinates.

@@ -343,6 +343,84 @@ struct SoftState {
 template <int D, bool TMA>
 constexpr int kCtasPerSm = (D == 64) ? 4 : 3;
 
+// Per-head coefficients of the attention mass from the (max, sum) pairs of a
+// KV head's g query heads (fin[h] = max, fin[8 + h] = sum):
+// ML[h] = max * log2(e), iL[h] = 1 / sum.
+__device__ __forceinline__ void mass_coeffs(const float* fin, int g, float (&ML)[8], float (&iL)[8]) {
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    ML[h] = (h < g) ? fin[h] * kL2E : 0.0f;
+    iL[h] = (h < g) ? 1.0f / fin[8 + h] : 0.0f;
+  }
+}
+
+// One head's share of a token's mass, exp(s - max) / sum, added to acc: the
+// same expression as the attention's own mass epilogue (which contracts the
+// product and the sum into one fused multiply-add), so that the deferred
+// mass of per-layer steps has the bits of a whole step's (checked bitwise
+// by the per-layer tests).
+__device__ __forceinline__ float mass_term(float acc, float s, float ml, float il) {
+  return acc + ex2(fmaf(s, kL2E, -ml)) * il;
+}
+
+// Attention mass of the tokens [lo[r], hi[r]) of both regions (r = 0 INT8,
+// 1 FP16) of one unit, summed over its g query heads, from the raw scores SC
+// (g rows of `slots`) into MS.  Both regions start 16-byte aligned (cap8 % 32
+// == 0, slots % 16 == 0), so four consecutive tokens of a head are one
+// 128-bit load.  Score lines are dropped from L2 once read.  Called by all
+// kThreads threads of the CTA.
+__device__ __forceinline__ void mass_rows(const float* SC, float* MS, int slots, int cap8, int g,
+                                          const float (&ML)[8], const float (&iL)[8],
+                                          const int (&lo)[2], const int (&hi)[2]) {
+  const int tid = threadIdx.x;
+  for (int region = 0; region < 2; ++region) {
+    const int base = region ? cap8 : 0;
+    const int jlo = lo[region] >> 2, jhi = (hi[region] + 3) >> 2;   // float4 groups of 4 tokens
+    // two float4 rows of every head per thread in flight; j runs from a
+    // multiple of 8 so that the 8 groups of a 128-byte line sit in one warp
+    for (int j0 = (jlo & ~7) + tid; j0 < jhi; j0 += 2 * kThreads) {
+      float4 sv[2][8];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int j = j0 + u * kThreads;
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+          if (h < g && j >= jlo && j < jhi)
+            sv[u][h] = __ldcg(reinterpret_cast<const float4*>(SC + static_cast<size_t>(h) * slots + base) + j);
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int j = j0 + u * kThreads;
+        if (j < jlo || j >= jhi) continue;
+        float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+          if (h < g) {
+            a.x = mass_term(a.x, sv[u][h].x, ML[h], iL[h]);
+            a.y = mass_term(a.y, sv[u][h].y, ML[h], iL[h]);
+            a.z = mass_term(a.z, sv[u][h].z, ML[h], iL[h]);
+            a.w = mass_term(a.w, sv[u][h].w, ML[h], iL[h]);
+          }
+        // The raw scores are dead once read here (the next step rewrites every
+        // live slot before reading it): drop whole 128-byte lines of them from
+        // L2 so they are never written back.  The 8 lanes reading one line are
+        // in this warp; lines shared with a neighbouring row are kept.
+        __syncwarp(__activemask());
+        if ((j & 7) == 0 && 4 * j + 32 <= hi[region]) {
+#pragma unroll
+          for (int h = 0; h < 8; ++h)
+            if (h < g) {
+              const float* line = SC + static_cast<size_t>(h) * slots + base + 4 * j;
+              if ((reinterpret_cast<uintptr_t>(line) & 127u) == 0) l2_discard_line(line);
+            }
+        }
+        // slots past the region end hold stale scores; their mass is never read
+        reinterpret_cast<float4*>(MS + base)[j] = a;
+      }
+    }
+  }
+}
+
 template <int D, bool TMA, bool CH>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm<D, TMA>)
 k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
@@ -471,8 +549,10 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   for (int mt = 0; mt < G::KS; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.0f;
   SoftState ss{-INFINITY, -INFINITY, 0.0f, 0.0f, 0.0f, 0.0f, 0};
   float* SC = c.scores + (static_cast<size_t>(lb) * c.Hq + kvh * g) * c.slots;
-  // raw scores are kept (for the mass epilogue) only when the policy uses them
-  const bool wA = ap.mass && 2 * t4 < g, wB = ap.mass && 2 * t4 + 1 < g;
+  // raw scores are kept (for the mass epilogue, now or deferred) only when
+  // the policy uses them
+  const bool keep_sc = ap.mass || ap.defer_mass;
+  const bool wA = keep_sc && 2 * t4 < g, wB = keep_sc && 2 * t4 + 1 < g;
 
   // one online-softmax update with a new scale exponent; returns 2^E
   auto update = [&](float mxA, float mxB, int Enew) -> float {
@@ -970,7 +1050,21 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     }
     if (tid == 0) ap.ticket[unit] = 0u;
   }
-  if (!ap.mass) return;       // the policy ranks without the attention mass
+  if (!ap.mass) {
+    // the policy ranks without the attention mass, or (per-layer steps) the
+    // mass is deferred: the raw scores and each head's (max, sum) are kept
+    // for the next step's first kernel (launch_mass_finalise)
+    if (ap.defer_mass) {
+      __syncthreads();
+      if ((!ap.cluster || split == 0) && tid < g) {
+        float* f = c.fin + (static_cast<size_t>(lb) * c.Hq + kvh * g + tid) * 2;
+        f[0] = fin[tid];
+        f[1] = fin[8 + tid];
+      }
+      if ((!ap.cluster || split == 0) && tid == 0) c.mass_pending[unit] = 1;
+    }
+    return;
+  }
   __syncthreads();
   // ---- attention mass of every token: sum over the group of p_{h,i} ----
   // Both regions start 16-byte aligned (cap8 % 32 == 0, slots % 16 == 0), so
@@ -1040,6 +1134,33 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       }
     }
   }
+}
+
+// The attention mass of the units whose per-layer launches deferred it: one
+// CTA per (layer, sequence, KV head), the same coefficients and arithmetic
+// as the attention's epilogue over every cached token.  The CTA clears the
+// unit's flag once done: the score lines it drops from L2 must never be read
+// again, so a second finalisation of the same step must do nothing.
+__global__ void __launch_bounds__(kThreads) k_mass_finalise(Cache c) {
+  pdl_trigger();     // the next kernel waits for this grid before it reads anything
+  pdl_wait();        // the attention launches that kept the scores are complete
+  const int unit = blockIdx.x, lb = unit / c.Hkv, kvh = unit - lb * c.Hkv, g = c.g;
+  if (!c.mass_pending[unit]) return;
+  const int n8 = c.n8[lb], n16 = c.n16[lb];
+  __shared__ float fin[16];
+  if (threadIdx.x < g) {
+    const float* f = c.fin + (static_cast<size_t>(lb) * c.Hq + kvh * g + threadIdx.x) * 2;
+    fin[threadIdx.x] = f[0];
+    fin[8 + threadIdx.x] = f[1];
+  }
+  __syncthreads();
+  float ML[8], iL[8];
+  mass_coeffs(fin, g, ML, iL);
+  const int lo[2] = {0, 0}, hi[2] = {n8, n16};
+  mass_rows(c.scores + (static_cast<size_t>(lb) * c.Hq + kvh * g) * c.slots,
+            c.mass + (static_cast<size_t>(lb) * c.Hkv + kvh) * c.slots, c.slots, c.cap8, g, ML, iL,
+            lo, hi);
+  if (threadIdx.x == 0) c.mass_pending[unit] = 0;     // only this CTA reads the unit's flag
 }
 
 // Self-test of the bounded wait: one thread waits on an mbarrier phase that
@@ -1188,6 +1309,12 @@ cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStrea
   if (c.d == 128)
     return ch ? launch_mma_staging<128, true>(c, ap, s) : launch_mma_staging<128, false>(c, ap, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_mass_finalise(const Cache& c, cudaStream_t s) {
+  const int units = c.L * c.B * c.Hkv;
+  const cudaError_t e = launch_pdl(k_mass_finalise, dim3(units), dim3(kThreads), 0, s, c);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t selftest_bounded_wait(unsigned long long limit_ns, int* gave_up,

@@ -220,8 +220,10 @@ int confkv_step(confkv_ctx* ctx, const float* logits, const uint16_t* q,
  * Per-layer stepping, for a model that produces one layer's q / k / v at a
  * time (the layers of a decode step are not all known up front):
  *
- * confkv_step_begin -- first stage of a decode step: the confidence and the
- * budget of every sequence from this step's logits (as in confkv_step), then
+ * confkv_step_begin -- first stage of a decode step: the attention mass the
+ * previous per-layer step deferred (a no-op where nothing is pending), the
+ * confidence and the budget of every sequence from this step's logits (as in
+ * confkv_step), then
  * the EMA update, ranking, eviction, compaction and INT8 aging of every
  * layer's caches in one launch (none of it depends on the new token's K/V),
  * reserving each layer's FP16 slot for its arriving token.
@@ -237,6 +239,12 @@ int confkv_step(confkv_ctx* ctx, const float* logits, const uint16_t* q,
  * Every layer must be run exactly once, in any order; the step (and the
  * position) advances after the last one.  Until a layer has run, its caches
  * hold the step's compacted state without the arriving token's K/V rows.
+ * On the tensor-core attention a layer's launch ends with its output and
+ * keeps the raw scores and each query head's (max, sum); the per-token
+ * attention mass that the next step ranks by is computed from them by the
+ * next confkv_step_begin (or confkv_step, confkv_step_host, or a
+ * confkv_read_cache that asks for the mass), with the same arithmetic as a
+ * whole step, so the results stay bitwise equal.
  * CONFKV_ERR_STATE without a begun step or for a layer already run;
  * CONFKV_ERR_INVALID_ARG for a bad layer.  The results equal confkv_step's
  * for the same inputs.

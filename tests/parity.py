@@ -126,6 +126,9 @@ def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, spli
     spread: optional per-channel powers of two (length d) multiplying every
       K (and, reversed, every V) row of the prefill and of each step, on both
       sides identically.
+    per_layer: True runs every step through confkv_step_begin + one
+      confkv_step_layer per layer (reversed order); a callable s -> bool
+      chooses per step (mixed per-layer and whole steps).
     """
     sk = None if spread is None else np.asarray(spread, np.float32)
     sv = None if spread is None else sk[::-1].copy()
@@ -193,7 +196,8 @@ def run(w, steps=None, lbs=None, device_inputs=False, check_codes_every=16, spli
                 gk, gv = _spread_dev(gk, sk), _spread_dev(gv, sv)
         else:
             glg, gq, gk, gv = (to_dev(x, dev) for x in (lg, q, k, v))
-        if per_layer:        # confkv_step_begin + one confkv_step_layer per layer, reversed
+        if per_layer is True or (callable(per_layer) and per_layer(s)):
+            # confkv_step_begin + one confkv_step_layer per layer, reversed
             kv.step_begin(glg, cf, bd)
             for l in reversed(range(w.L)):
                 ol = torch.empty(w.B, w.Hq, w.d, device=dev)

@@ -66,6 +66,15 @@ def test_per_layer_parity_with_oracle():
     parity.check(parity.run(small(L=4, Hq=40, Hkv=8, steps=25), per_layer=True))
 
 
+@pytest.mark.parametrize("splits", [0, 1, 12])
+def test_mixed_per_layer_and_whole_steps(splits):
+    # per-layer launches defer each layer's attention mass to the next step's
+    # first kernel; whole steps after per-layer steps (and the reverse) must
+    # fold it in exactly as if every step had been whole
+    w = small(L=3, Hq=40, Hkv=8, steps=30)
+    parity.check(parity.run(w, splits=splits, per_layer=lambda s: (s // 4) % 2 == 0))
+
+
 def test_per_layer_state_errors():
     import confidence_gated_kv_logits_gb300 as pkg
     w = small()
@@ -176,3 +185,37 @@ def test_step_graph_replayed_equals_eager(per_layer, policy):
         if a.dtype == np.float32:
             a, b = a.view(np.uint32), b.view(np.uint32)
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("ch,splits", [(0, 1), (1, 1), (0, 2), (1, 2)])
+def test_per_layer_cache_state_equals_whole_step(ch, splits):
+    # Per-layer launches defer each layer's attention mass to the next
+    # step's first kernel (or to an inspection of the cache).  Reading the
+    # caches lane by lane between steps finalises the masses repeatedly,
+    # which must change nothing: every lane's positions, EMA, mass, codes,
+    # scales and FP16 rows equal those of whole steps on the same inputs.
+    import confidence_gated_kv_logits_gb300 as pkg
+    w = small(L=3, Hq=40, Hkv=8, prefill=70, steps=8, int8_channel=ch)
+    a = pkg.ConfKV.for_workload(w, device=0, attn_splits=splits)
+    b = pkg.ConfKV.for_workload(w, device=0, attn_splits=splits)
+    kvs = [[wl.prefill_kv_lb(w, l, bb) for bb in range(w.B)] for l in range(w.L)]
+    K = np.stack([np.stack([x[0] for x in row]) for row in kvs])
+    V = np.stack([np.stack([x[1] for x in row]) for row in kvs])
+    a.prefill(_T(K), _T(V), w.prefill)
+    b.prefill(_T(K), _T(V), w.prefill)
+    for s in range(w.steps):
+        lg, q, k, v = (_T(x) for x in wl.step_inputs(w, s))
+        oa = torch.empty(w.L, w.B, w.Hq, w.d, device=DEV)
+        a.step(lg, q, k, v, oa)
+        b.step_begin(lg)
+        for l in reversed(range(w.L)):
+            ob = torch.empty(w.B, w.Hq, w.d, device=DEV)
+            b.step_layer(l, q[l].contiguous(), k[l].contiguous(), v[l].contiguous(), ob)
+            assert torch.equal(ob, oa[l]), (s, l)
+        for l in range(w.L):
+            for bb in range(w.B):
+                ra, rb = a.read_cache(l, bb), b.read_cache(l, bb)
+                for key in ("pos", "ema", "mass", "k8", "v8", "ks", "vs", "k16", "v16"):
+                    assert np.array_equal(ra[key], rb[key]), (s, l, bb, key)
+    a.close()
+    b.close()
