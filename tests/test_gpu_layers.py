@@ -62,8 +62,12 @@ def test_per_layer_equals_full_step_bitwise(d, splits, kernel):
     b.close()
 
 
-def test_per_layer_parity_with_oracle():
-    parity.check(parity.run(small(L=4, Hq=40, Hkv=8, steps=25), per_layer=True))
+@pytest.mark.parametrize("policy", [0, 2])
+def test_per_layer_parity_with_oracle(policy):
+    # both policies that rank by the attention mass (CONF-KV's EMA, H2O's
+    # accumulated mass) defer it under per-layer stepping
+    parity.check(parity.run(small(L=4, Hq=40, Hkv=8, steps=25), per_layer=True, policy=policy,
+                            seed=7))
 
 
 @pytest.mark.parametrize("splits", [0, 1, 12])
