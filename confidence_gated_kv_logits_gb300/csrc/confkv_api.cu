@@ -796,11 +796,12 @@ int confkv_read_cache(confkv_ctx* c, int l, int b, int cap, int* n8o, int* n16o,
   if (!c || l < 0 || l >= c->L || b < 0 || b >= c->B || cap < 0)
     return fail(c, CONFKV_ERR_INVALID_ARG, "bad (l, b) or cap");
   DeviceGuard guard(c->device);
-  if (mass && c->layered && uses_mass(c) && !c->step_open) {
+  cudaError_t e = cudaDeviceSynchronize();     // the caller's steps may be on any stream
+  if (e == cudaSuccess && mass && c->layered && uses_mass(c) && !c->step_open) {
     const int rc = run_mass_finalise(c, nullptr);     // deferred masses first
     if (rc != CONFKV_OK) return rc;
+    e = cudaDeviceSynchronize();
   }
-  cudaError_t e = cudaDeviceSynchronize();
   const size_t lb = static_cast<size_t>(l) * c->B + b;
   int n8 = 0, n16 = 0;
   if (e == cudaSuccess) e = cudaMemcpy(&n8, c->cache.n8 + lb, 4, cudaMemcpyDeviceToHost);
