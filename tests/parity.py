@@ -32,7 +32,8 @@ RECORDS = []        # (test id, Report) of every run in this process
 
 
 def to_dev(a, dev):
-    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    # a writable, contiguous host copy: some generators hand out read-only views
+    return torch.from_numpy(np.require(a, requirements=("C", "W"))).to(dev)
 
 
 class Report:

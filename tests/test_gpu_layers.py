@@ -223,3 +223,40 @@ def test_per_layer_cache_state_equals_whole_step(ch, splits):
                     assert np.array_equal(ra[key], rb[key]), (s, l, bb, key)
     a.close()
     b.close()
+
+
+def test_read_cache_after_per_layer_steps_on_a_side_stream():
+    # the caller's per-layer steps run on a non-blocking stream; reading the
+    # caches right after them (no host synchronisation in between) must see
+    # the finished step, its deferred masses included
+    import confidence_gated_kv_logits_gb300 as pkg
+    w = small(L=2, Hq=40, Hkv=8, prefill=70, steps=5)
+    a = pkg.ConfKV.for_workload(w, device=0)
+    b = pkg.ConfKV.for_workload(w, device=0)
+    kvs = [[wl.prefill_kv_lb(w, l, bb) for bb in range(w.B)] for l in range(w.L)]
+    K = _T(np.stack([np.stack([x[0] for x in row]) for row in kvs]))
+    V = _T(np.stack([np.stack([x[1] for x in row]) for row in kvs]))
+    a.prefill(K, V, w.prefill)
+    b.prefill(K, V, w.prefill)
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for s in range(w.steps):
+        lg, q, k, v = (_T(x) for x in wl.step_inputs(w, s))
+        oa = torch.empty(w.L, w.B, w.Hq, w.d, device=DEV)
+        a.step(lg, q, k, v, oa)
+        side.wait_stream(torch.cuda.current_stream())      # the inputs are ready
+        with torch.cuda.stream(side):
+            ob = torch.empty(w.L, w.B, w.Hq, w.d, device=DEV)
+            b.step_begin(lg, stream=side)
+            for l in range(w.L):
+                b.step_layer(l, q[l].contiguous(), k[l].contiguous(), v[l].contiguous(), ob[l],
+                             stream=side)
+        for l in range(w.L):
+            for bb in range(w.B):
+                ra, rb = a.read_cache(l, bb), b.read_cache(l, bb)
+                for key in ("pos", "ema", "mass", "k8", "ks", "k16"):
+                    assert np.array_equal(ra[key], rb[key]), (s, l, bb, key)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob)
+    a.close()
+    b.close()
