@@ -205,9 +205,14 @@ int auto_splits_layer(int units, int ncap, int d, int sms) {
   return n > 1 ? (n & ~1) : 1;
 }
 
+// layer_call: 0 not a per-layer call; 1 the first layer launch of a
+// per-layer step; 2 a later one (which may read its cache before its wait)
 int run_attention(confkv_ctx* c, const __half* q, float* out, cudaStream_t s, int lb0, int nlb,
-                  int splits, const StepParams* fused = nullptr, bool defer_mass = false) {
+                  int splits, const StepParams* fused = nullptr, bool defer_mass = false,
+                  int layer_call = 0) {
   AttnParams ap{};
+  ap.q_late = layer_call != 0 ? 1 : 0;
+  ap.early = layer_call == 2 ? 1 : 0;
   if (fused) {
     ap.k_new = fused->k_new;
     ap.v_new = fused->v_new;
@@ -479,10 +484,10 @@ int run_select(confkv_ctx* c, const StepParams& sp, cudaStream_t s) {
 
 int run_attention_timed(confkv_ctx* c, const uint16_t* q, float* out, cudaStream_t s, int lb0,
                         int nlb, int splits, const StepParams* fused = nullptr,
-                        bool defer_mass = false) {
+                        bool defer_mass = false, int layer_call = 0) {
   prof_mark(c, 3, s);
   const int rc = run_attention(c, reinterpret_cast<const __half*>(q), out, s, lb0, nlb, splits, fused,
-                               defer_mass);
+                               defer_mass, layer_call);
   prof_mark(c, 3, s);
   return rc;
 }
@@ -598,8 +603,10 @@ int confkv_step_layer(confkv_ctx* c, int layer, const uint16_t* q, const uint16_
   }
   // the tensor-core attention defers this layer's mass to the next step's
   // first kernel, so that the layer's launch ends with its output
+  // the step's first layer launch finds the selection possibly still running;
+  // every later one starts after that launch has waited for it
   rc = run_attention_timed(c, q, out, s, layer * c->B, c->B, c->splits_layer, fused ? &sp : nullptr,
-                           fused);
+                           fused, c->layers_left == c->L ? 1 : 2);
   if (rc != CONFKV_OK) return rc;
   c->layer_done[layer] = 1;
   if (--c->layers_left == 0) {

@@ -160,6 +160,16 @@ struct AttnParams {
   const __half* v_new;
   int32_t* kept_pos;
   int32_t* kept_count;
+  // Per-layer calls: the caller's q, k_new and v_new may come from the kernel
+  // right before this launch, so they are read only after the dependency
+  // wait (q_late = 1).  A layer launch that is not the step's first may also
+  // read its own layer's cache (region sizes, reserved slot, tiles) before
+  // the wait (early = 1, tensor-core TMA path): that cache is written only by
+  // the step's selection, which is complete by then -- the step's first
+  // layer launch passes its own wait (the selection done) before it
+  // triggers, and every later launch in the stream starts after that trigger.
+  int q_late;
+  int early;
 };
 
 // ---- launch wrappers (each file owns its kernels) ----

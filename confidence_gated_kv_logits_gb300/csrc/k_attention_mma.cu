@@ -34,7 +34,11 @@
 // first chunk -- an INT8 chunk whenever the unit holds enough of them --
 // before it reads the region sizes, so that the two round trips of the
 // prologue overlap.  Under per-layer stepping the kept positions of a
-// (layer, sequence) are copied by all of its CTAs, one slice each.
+// (layer, sequence) are copied by all of its CTAs, one slice each, and every
+// layer launch but the step's first reads its region sizes and requests its
+// first tiles before its dependency wait (its layer's cache is final once
+// the step's selection is done), so that they arrive while the previous
+// launch finishes; the caller's q, k_new and v_new are read after the wait.
 //
 // Per-(head, channel) storage mode (CH): an INT8 element reads as
 // code * s * 2^f_c.  For K the channel factors go into the query (q_c 2^f_c,
@@ -421,7 +425,10 @@ __device__ __forceinline__ void mass_rows(const float* SC, float* MS, int slots,
   }
 }
 
-template <int D, bool TMA, bool CH>
+// PL: launches that store the arriving token's K/V rows themselves
+// (AttnParams::k_new set: per-layer steps and host steps); whole steps
+// (the selection stored the token) run the instance without that code.
+template <int D, bool TMA, bool CH, bool PL>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm<D, TMA>)
 k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   using G = Geo<D>;
@@ -456,76 +463,127 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       for (int kk = 0; kk < G::KS; ++kk) qb[kk][0] = qb[kk][1] = 0u;
     }
   };
-  load_q();
-
-  // everything below reads the selection kernel's results
-  pdl_wait();
-  if constexpr (CH) {
-    // the INT8 chunks' query: channel c times 2^f_c of this KV head's K
-    const int8_t* fk = c.chexp + static_cast<size_t>(unit) * 2 * D + t4 * G::KPT;
+  // CH: the INT8 chunks' query is channel c times 2^f_c of this KV head's K
+  auto scale_q_channels = [&]() {
+    if constexpr (CH) {
+      const int8_t* fk = c.chexp + static_cast<size_t>(unit) * 2 * D + t4 * G::KPT;
 #pragma unroll
-    for (int kk = 0; kk < G::KS; ++kk) {
-      const uint32_t e4 = *reinterpret_cast<const uint32_t*>(fk + 4 * kk);
-      uint32_t fac[2];
+      for (int kk = 0; kk < G::KS; ++kk) {
+        const uint32_t e4 = *reinterpret_cast<const uint32_t*>(fk + 4 * kk);
+        uint32_t fac[2];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int f0 = static_cast<int8_t>((e4 >> (16 * hh)) & 0xffu);
-        const int f1 = static_cast<int8_t>((e4 >> (16 * hh + 8)) & 0xffu);
-        // fp16 2^f: exponent field f + 15 (f in [-8, 0]: normal)
-        fac[hh] = (static_cast<uint32_t>(f0 + 15) << 10) | (static_cast<uint32_t>(f1 + 15) << 26);
-      }
+        for (int hh = 0; hh < 2; ++hh) {
+          const int f0 = static_cast<int8_t>((e4 >> (16 * hh)) & 0xffu);
+          const int f1 = static_cast<int8_t>((e4 >> (16 * hh + 8)) & 0xffu);
+          // fp16 2^f: exponent field f + 15 (f in [-8, 0]: normal)
+          fac[hh] = (static_cast<uint32_t>(f0 + 15) << 10) | (static_cast<uint32_t>(f1 + 15) << 26);
+        }
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        __half2 qv = *reinterpret_cast<__half2*>(&qb[kk][hh]);
-        qv = __hmul2(qv, *reinterpret_cast<const __half2*>(&fac[hh]));
-        qb[kk][hh] = *reinterpret_cast<uint32_t*>(&qv);
+        for (int hh = 0; hh < 2; ++hh) {
+          __half2 qv = *reinterpret_cast<__half2*>(&qb[kk][hh]);
+          qv = __hmul2(qv, *reinterpret_cast<const __half2*>(&fac[hh]));
+          qb[kk][hh] = *reinterpret_cast<uint32_t*>(&qv);
+        }
       }
     }
-  }
+  };
   const uint32_t wbase = smem_u32(smem) + warp * kStages * STAGE;
-  // Speculative first tile (TMA, one split, whole steps): warp w's first
-  // chunk is chunk w, an INT8 chunk whenever the unit holds more than w INT8
-  // chunks (every unit of a long context).  Its tiles are requested before
-  // the region sizes are read, so that the two round trips overlap; a wrong
-  // guess costs one wasted tile and shifts the warp's stage sequence by one.
-  // The guard keeps the tile inside the INT8 arrays for every unit.
-  bool spec = false;
   if constexpr (TMA) {
     if (lane == 0)
       for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     __syncwarp();
-    spec = ap.splits == 1 && !ap.k_new && c.cap8 >= 32 * kWarps;
-    if (spec && lane == 0) {
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      issue_chunk_tma<D>(c, tm, unit, 0x7fffffff, warp, wbase, smem_u32(&bars[warp][0]));
-    }
   }
-  const int n8 = c.n8[lb], n16 = c.n16[lb];
+  // Region sizes, chunk range and the reserved slot of the arriving token
+  // (per-layer steps: hn, in the chunk cf of one CTA, that warp's chunk
+  // index hold).  An early launch reads them, and requests the tiles of its
+  // first kStages chunks (all but the reserved slot's chunk, whose tiles
+  // wait for the token's rows), before its dependency wait.
+  const bool early = PL && TMA && ap.early != 0;
+  int n8 = 0, n16 = 0, hn = -1;
+  int nis = 0;                 // chunks of this warp requested before the main loop's own requests
+  bool spec = false;
+  if (early) {
+    n8 = __ldcg(c.n8 + lb);
+    n16 = __ldcg(c.n16 + lb);
+    hn = __ldcg(c.new_slot + lb);
+  } else {
+    // whole steps: q's producer precedes the step's first kernel, which waits
+    // for it before it triggers, so q is complete when this grid starts
+    if (!PL || !ap.q_late) load_q();
+    // everything below reads the selection kernel's results
+    pdl_wait();
+    if (PL && ap.q_late) load_q();
+    scale_q_channels();
+    // Speculative first tile (TMA, one split, whole steps): warp w's first
+    // chunk is chunk w, an INT8 chunk whenever the unit holds more than w INT8
+    // chunks (every unit of a long context).  Its tiles are requested before
+    // the region sizes are read, so that the two round trips overlap; a wrong
+    // guess costs one wasted tile and shifts the warp's stage sequence by one.
+    // The guard keeps the tile inside the INT8 arrays for every unit.
+    if constexpr (TMA) {
+      spec = !PL && ap.splits == 1 && c.cap8 >= 32 * kWarps;
+      if (spec && lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        issue_chunk_tma<D>(c, tm, unit, 0x7fffffff, warp, wbase, smem_u32(&bars[warp][0]));
+      }
+    }
+    n8 = c.n8[lb];
+    n16 = c.n16[lb];
+    if (PL) hn = c.new_slot[lb];
+  }
   const int nc8 = (n8 + 31) >> 5, nc16 = (n16 + 15) >> 4, nc = nc8 + nc16;
   const int cb = static_cast<int>(static_cast<long long>(nc) * split / ap.splits);
   const int ce = static_cast<int>(static_cast<long long>(nc) * (split + 1) / ap.splits);
   const int cnt = (ce - cb > warp) ? (ce - cb - warp + kWarps - 1) / kWarps : 0;
+  const int cf = hn >= 0 ? nc8 + (hn >> 4) : -1;
+  const bool covers_new = PL && cf >= cb && cf < ce;
+  // Per-layer steps: the kept positions of this (layer, sequence), INT8
+  // slots then FP16 slots, are copied by all its CTAs, slice [k0, k1) each
+  // (loads before stores); an early launch loads its first kThreads before
+  // its wait.  The copy precedes the main loop, off the merge's path.
+  auto kept_slice = [&](int& k0, int& k1) {
+    const int parts = ap.splits * c.Hkv, part = split * c.Hkv + kvh, n = n8 + n16;
+    const int per = (n + parts - 1) / parts;
+    k0 = part * per;
+    k1 = min(n, k0 + per);
+  };
+  int kpre = 0;
+  if (early) {
+    int hold = kStages;
+    if (covers_new && (cf - cb) % kWarps == warp) hold = min(hold, (cf - cb) / kWarps);
+    if (lane == 0)
+      for (int i = 0; i < min(hold, cnt); ++i) {
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        issue_chunk_tma<D>(c, tm, unit, nc8, cb + warp + kWarps * i, wbase + i * STAGE,
+                           smem_u32(&bars[warp][i]));
+      }
+    nis = hold;
+    int k0, k1;
+    kept_slice(k0, k1);
+    if (PL && ap.kept_pos && k0 + tid < k1)
+      kpre = (k0 + tid < n8) ? __ldcg(c.pos8 + static_cast<size_t>(lb) * c.cap8 + k0 + tid)
+                             : __ldcg(c.pos16 + static_cast<size_t>(lb) * c.Wr + k0 + tid - n8);
+    pdl_wait();
+    load_q();
+    scale_q_channels();
+  }
   // Per-layer steps: the selection ran ahead and reserved FP16 slot hn for the
   // arriving token.  The one CTA whose chunk range holds that slot stores the
-  // token's K/V rows of this KV head before any of its tiles is read.
-  if (ap.k_new) {
-    const int hn = c.new_slot[lb];
-    const int cf = nc8 + (hn >> 4);
-    if (cf >= cb && cf < ce) {
-      const size_t src = (static_cast<size_t>(lbu) * c.Hkv + kvh) * D;
-      const size_t dst = (static_cast<size_t>(unit) * c.Wr + hn) * D;
-      for (int it = tid; it < D / 4; it += kThreads) {     // D/8 16-byte pieces of K, then V
-        const bool isv = it >= D / 8;
-        const int ch = isv ? it - D / 8 : it;
-        reinterpret_cast<int4*>((isv ? c.v16 : c.k16) + dst)[ch] =
-            reinterpret_cast<const int4*>((isv ? ap.v_new : ap.k_new) + src)[ch];
-      }
-      // the tiles are read by TMA (the async proxy): order the generic stores first
-      if constexpr (TMA) asm volatile("fence.proxy.async.global;\n" ::: "memory");
-      __syncthreads();
-      if constexpr (TMA) asm volatile("fence.proxy.async.global;\n" ::: "memory");
+  // token's K/V rows of this KV head before that slot's tiles are requested.
+  if (covers_new) {
+    const size_t src = (static_cast<size_t>(lbu) * c.Hkv + kvh) * D;
+    const size_t dst = (static_cast<size_t>(unit) * c.Wr + hn) * D;
+    for (int it = tid; it < D / 4; it += kThreads) {     // D/8 16-byte pieces of K, then V
+      const bool isv = it >= D / 8;
+      const int ch = isv ? it - D / 8 : it;
+      reinterpret_cast<int4*>((isv ? c.v16 : c.k16) + dst)[ch] =
+          reinterpret_cast<const int4*>((isv ? ap.v_new : ap.k_new) + src)[ch];
     }
+    // the tiles are read by TMA (the async proxy): order the generic stores first
+    if constexpr (TMA) asm volatile("fence.proxy.async.global;\n" ::: "memory");
+    __syncthreads();
+    if constexpr (TMA) asm volatile("fence.proxy.async.global;\n" ::: "memory");
   }
   bool ok_all = true;
   int fail_i = 0;
@@ -668,7 +726,33 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   };
 #pragma unroll
   for (int i = 0; i < kStages - 1; ++i)
-    if (!(spec_hit && i == 0)) issue(i);                 // chunk 0 may be in flight already
+    if (!(spec_hit && i == 0) && i >= nis) issue(i);     // chunk 0 may be in flight already
+  if (PL && ap.kept_pos) {
+    const int32_t* __restrict__ kpos8 = c.pos8 + static_cast<size_t>(lb) * c.cap8;
+    const int32_t* __restrict__ kpos16 = c.pos16 + static_cast<size_t>(lb) * c.Wr;
+    int32_t* __restrict__ kp = ap.kept_pos + static_cast<size_t>(lbu) * c.Ncap;
+    int k0, k1;
+    kept_slice(k0, k1);
+    int base = k0;
+    if (early) {
+      if (k0 + tid < k1) kp[k0 + tid] = kpre;
+      base += kThreads;
+    }
+    for (; base < k1; base += 4 * kThreads) {
+      int v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * kThreads + tid;
+        v[u] = (i < k1) ? ((i < n8) ? kpos8[i] : kpos16[i - n8]) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * kThreads + tid;
+        if (i < k1) kp[i] = v[u];
+      }
+    }
+  }
+  if (PL && split == 0 && kvh == 0 && ap.kept_count && tid == 0) ap.kept_count[lbu] = n8 + n16;
   for (int i = 0; i < (ok_all ? cnt : 0); ++i) {
     if constexpr (TMA) {
       // every lane waits (each needs the wait's acquire of the tile), and the
@@ -684,7 +768,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       cp_wait<kStages - 2>();
     }
     __syncwarp();
-    issue(i + kStages - 1);
+    if (i + kStages - 1 >= nis) issue(i + kStages - 1);
     const int ci = cb + warp + kWarps * i;
     const uint32_t st = wbase + ((i + so) % kStages) * STAGE;
     if constexpr (CH) {
@@ -868,40 +952,19 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     if (!v_scaled) scale_v_channels();     // the warp's chunks were all INT8 (or none)
   }
   pdl_trigger();     // the next kernel in the stream may be scheduled
-  if (ap.kept_pos) {
-    // per-layer steps: the kept positions of this (layer, sequence), INT8
-    // slots then FP16 slots, copied by all its CTAs (one slice each, every
-    // thread's loads issued before its stores)
-    const int32_t* __restrict__ pos8 = c.pos8 + static_cast<size_t>(lb) * c.cap8;
-    const int32_t* __restrict__ pos16 = c.pos16 + static_cast<size_t>(lb) * c.Wr;
-    int32_t* __restrict__ kp = ap.kept_pos + static_cast<size_t>(lbu) * c.Ncap;
-    const int parts = ap.splits * c.Hkv, part = split * c.Hkv + kvh, n = n8 + n16;
-    const int per = (n + parts - 1) / parts;
-    const int i0 = part * per, i1 = min(n, i0 + per);
-    for (int base = i0; base < i1; base += 4 * kThreads) {
-      int v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = base + u * kThreads + tid;
-        v[u] = (i < i1) ? ((i < n8) ? pos8[i] : pos16[i - n8]) : 0;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = base + u * kThreads + tid;
-        if (i < i1) kp[i] = v[u];
-      }
-    }
-  }
-  if (split == 0 && kvh == 0 && ap.kept_count && tid == 0) ap.kept_count[lbu] = n8 + n16;
   if (!ok_all) {
     // a tile never arrived: flag the step (its output for this unit is
     // incomplete) and give the copy in flight one more bounded wait before
     // the shared memory is reused
     if (lane == 0) atomicOr(c.err, 4);
-    if (fail_i >= 0)
-      mbar_wait(smem_u32(&bars[warp][(fail_i + so) % kStages]), ((fail_i + so) / kStages) & 1);
-    else
+    if (fail_i >= 0) {
+      // the chunk waited for and, after an early launch's requests, the next
+      const int last = min(cnt, max(fail_i + 1, nis));
+      for (int j = fail_i; j < last; ++j)
+        mbar_wait(smem_u32(&bars[warp][(j + so) % kStages]), ((j + so) / kStages) & 1);
+    } else {
       mbar_wait(smem_u32(&bars[warp][0]), 0);      // the wasted speculative tile
+    }
   }
 
   // ---- merge the warps of this CTA (shared memory reused) ----
@@ -1054,7 +1117,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     // the policy ranks without the attention mass, or (per-layer steps) the
     // mass is deferred: the raw scores and each head's (max, sum) are kept
     // for the next step's first kernel (launch_mass_finalise)
-    if (ap.defer_mass) {
+    if (PL && ap.defer_mass) {
       __syncthreads();
       if ((!ap.cluster || split == 0) && tid < g) {
         float* f = c.fin + (static_cast<size_t>(lb) * c.Hq + kvh * g + tid) * 2;
@@ -1177,7 +1240,7 @@ __global__ void k_selftest_wait(unsigned long long limit_ns, int* gave_up, unsig
   *gave_up = ok ? 0 : 1;
 }
 
-template <int D, bool TMA, bool CH>
+template <int D, bool TMA, bool CH, bool PL>
 cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm, cudaStream_t s) {
   const int smem = kWarps * kStages * (TMA ? kTmaStage<D> : Geo<D>::STAGE) + (TMA ? 1024 : 0);
   // per-device caches of the function attribute and of the cluster check
@@ -1187,7 +1250,7 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesCached) dev = -1;
   static bool attr_set[kMaxDevicesCached] = {};
   if (dev < 0 || !attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(k_attn_mma<D, TMA, CH>,
+    const cudaError_t e = cudaFuncSetAttribute(k_attn_mma<D, TMA, CH, PL>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0) attr_set[dev] = true;
@@ -1218,7 +1281,7 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
       q.attrs = at + 1;
       q.numAttrs = 1;
       int n = 0;
-      const cudaError_t oe = cudaOccupancyMaxActiveClusters(&n, k_attn_mma<D, TMA, CH>, &q);
+      const cudaError_t oe = cudaOccupancyMaxActiveClusters(&n, k_attn_mma<D, TMA, CH, PL>, &q);
       ok[ap.splits] = (oe == cudaSuccess && n > 0) ? 1 : -1;
       if (oe != cudaSuccess) (void)cudaGetLastError();
     }
@@ -1227,7 +1290,7 @@ cudaError_t launch_mma_d(const Cache& c, const AttnParams& ap, const TmaMaps& tm
       cfg.numAttrs = 2;
     }
   }
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_mma<D, TMA, CH>, c, a, tm);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_mma<D, TMA, CH, PL>, c, a, tm);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -1296,10 +1359,12 @@ cudaError_t launch_mma_staging(const Cache& c, const AttnParams& ap, cudaStream_
   TmaMaps tm;
   if (ap.tmaps) {
     std::memcpy(&tm, ap.tmaps, sizeof(tm));
-    return launch_mma_d<D, true, CH>(c, ap, tm, s);
+    return ap.k_new ? launch_mma_d<D, true, CH, true>(c, ap, tm, s)
+                    : launch_mma_d<D, true, CH, false>(c, ap, tm, s);
   }
   std::memset(&tm, 0, sizeof(tm));
-  return launch_mma_d<D, false, CH>(c, ap, tm, s);
+  return ap.k_new ? launch_mma_d<D, false, CH, true>(c, ap, tm, s)
+                  : launch_mma_d<D, false, CH, false>(c, ap, tm, s);
 }
 
 cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStream_t s) {
