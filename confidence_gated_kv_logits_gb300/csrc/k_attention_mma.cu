@@ -48,11 +48,17 @@
 // and the raw query is loaded again for the FP16 chunks.
 //
 // Split-K: with 2..8 splits the splits of a unit form one thread-block
-// cluster and merge through distributed shared memory: after a cluster
-// barrier every CTA reads the others' (max, sum) per head, computes its share
-// of the output from their partial accumulators and the attention mass of its
-// own tokens.  With more splits the partials go through global memory and the
-// CTA taking the last ticket finishes the unit.
+// cluster and merge through distributed shared memory.  Whole steps: after a
+// cluster barrier every CTA reads the others' (max, sum) per head, computes
+// its share of the output from their partial accumulators and the attention
+// mass of its own tokens.  Launches that store the arriving token (per-layer
+// steps, where the merge is on each layer's critical path) push instead:
+// each CTA signals the end of its main loop on the cluster barrier, merges
+// its warps, waits for the others' signal and writes its per-head (max, sum)
+// into every CTA and its partial of each output block into the CTA that
+// finishes that block; one more cluster barrier, and every read is local.
+// With more splits the partials go through global memory and the CTA taking
+// the last ticket finishes the unit.
 #include <cooperative_groups.h>
 #include <cuda.h>
 
@@ -967,96 +973,218 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     }
   }
 
-  // ---- merge the warps of this CTA (shared memory reused) ----
-  ss.lA = gsum8(ss.lA);
-  ss.lB = gsum8(ss.lB);
-  remove_offset();
-  __syncthreads();
+  // ---- merge the warps of this CTA (shared memory reused); then, with
+  // split-K, the splits of the unit ----
   float* wm = reinterpret_cast<float*>(smem);            // [kWarps][8]
   float* wl = wm + kWarps * 8;                           // [kWarps][8]
   float* fin = wl + kWarps * 8;                          // [2][8]
   float* wo = fin + 16;                                  // [kWarps][8][D]
-  float* cml = wo + kWarps * 8 * D;                      // cluster: this split's [2][8] max, sum
-  float* cacc = cml + 16;                                // cluster: this split's [8][D] output
-  const float unscale = pow2i(-ss.E);
-  if (gid == 0) {
-    wm[warp * 8 + 2 * t4] = ss.mA;
-    wm[warp * 8 + 2 * t4 + 1] = ss.mB;
-    wl[warp * 8 + 2 * t4] = ss.lA;
-    wl[warp * 8 + 2 * t4 + 1] = ss.lB;
-  }
-#pragma unroll
-  for (int mt = 0; mt < G::KS; ++mt) {
-    const int d0 = gid * G::VPT + 2 * mt;
-    float* oa = wo + (warp * 8 + 2 * t4) * D;
-    float* ob = oa + D;
-    oa[d0] = O[mt][0] * unscale;
-    ob[d0] = O[mt][1] * unscale;
-    oa[d0 + 1] = O[mt][2] * unscale;
-    ob[d0 + 1] = O[mt][3] * unscale;
-  }
-  __syncthreads();
   const size_t obase = static_cast<size_t>(lb) * c.Hq + kvh * g;     // split-K scratch
   float* outp = ap.out + (static_cast<size_t>(lbu) * c.Hq + kvh * g) * D;
-  for (int idx = tid; idx < g * D; idx += kThreads) {
-    const int h = idx / D, dd = idx - h * D;
-    float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 8 + h]);
-    float Ls = 0.0f, A = 0.0f;
-    for (int w = 0; w < kWarps; ++w) {
-      const float f = rescale(wm[w * 8 + h], M);
-      Ls += wl[w * 8 + h] * f;
-      A += wo[(w * 8 + h) * D + dd] * f;
+  if constexpr (PL) {
+    // Cluster: this CTA's tiles are all consumed; once every CTA of the
+    // cluster has said so, they write into each other's stage memory.
+    if (ap.cluster) asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+    ss.lA = gsum8(ss.lA);
+    ss.lB = gsum8(ss.lB);
+    remove_offset();
+    __syncthreads();
+    float* wf = wo + kWarps * 8 * D;                       // [kWarps][8]
+    // cluster: what the splits write into this CTA -- every split's per-head
+    // (max, sum) [S][2][8], and every split's partial of the output blocks this
+    // CTA finishes [S][jmax][kThreads] (output block k = k-th kThreads elements
+    // of the [g][D] output, finished by split k % S as its block k / S)
+    float* rml = wf + kWarps * 8;
+    float* racc = rml + kMaxClusterSplits * 16;
+    constexpr int kBlk = 8 * D / kThreads;                 // output blocks at most
+    const float unscale = pow2i(-ss.E);
+    if (gid == 0) {
+      wm[warp * 8 + 2 * t4] = ss.mA;
+      wm[warp * 8 + 2 * t4 + 1] = ss.mB;
+      wl[warp * 8 + 2 * t4] = ss.lA;
+      wl[warp * 8 + 2 * t4 + 1] = ss.lB;
     }
-    if (ap.splits == 1) {
-      outp[h * D + dd] = A / Ls;
-      if (dd == 0) { fin[h] = M; fin[8 + h] = Ls; }
-    } else if (ap.cluster) {
-      cacc[h * D + dd] = A;
-      if (dd == 0) { cml[h] = M; cml[8 + h] = Ls; }
-    } else {
-      const size_t pi = (obase + h) * ap.splits + split;
-      ap.part_acc[pi * D + dd] = A;
-      if (dd == 0) { ap.part_ml[pi * 2] = M; ap.part_ml[pi * 2 + 1] = Ls; }
+  #pragma unroll
+    for (int mt = 0; mt < G::KS; ++mt) {
+      const int d0 = gid * G::VPT + 2 * mt;
+      float* oa = wo + (warp * 8 + 2 * t4) * D;
+      float* ob = oa + D;
+      oa[d0] = O[mt][0] * unscale;
+      ob[d0] = O[mt][1] * unscale;
+      oa[d0 + 1] = O[mt][2] * unscale;
+      ob[d0 + 1] = O[mt][3] * unscale;
+    }
+    __syncthreads();
+    // per head: the CTA's (max, sum) and each warp's rescale factor to that max
+    float hM = 0.0f, hL = 0.0f;                            // thread tid < g: head tid's
+    if (tid < g) {
+      float M = -INFINITY;
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 8 + tid]);
+      float Ls = 0.0f;
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = rescale(wm[w * 8 + tid], M);
+        Ls += wl[w * 8 + tid] * f;
+        wf[w * 8 + tid] = f;
+      }
+      hM = M;
+      hL = Ls;
+      if (ap.splits == 1) {
+        fin[tid] = M;
+        fin[8 + tid] = Ls;
+      } else if (!ap.cluster) {
+        const size_t pi = (obase + tid) * ap.splits + split;
+        ap.part_ml[pi * 2] = M;
+        ap.part_ml[pi * 2 + 1] = Ls;
+      }
+    }
+    __syncthreads();
+    float Ab[kBlk];                                        // this thread's element of each block
+  #pragma unroll
+    for (int k = 0; k < kBlk; ++k) {
+      const int idx = k * kThreads + tid;
+      Ab[k] = 0.0f;
+      if (idx < g * D) {
+        const int h = idx / D, dd = idx - h * D;
+        float A = 0.0f;
+        for (int w = 0; w < kWarps; ++w) A += wo[(w * 8 + h) * D + dd] * wf[w * 8 + h];
+        Ab[k] = A;
+        if (ap.splits == 1) {
+          outp[h * D + dd] = A / fin[8 + h];
+        } else if (!ap.cluster) {
+          ap.part_acc[((obase + h) * ap.splits + split) * D + dd] = A;
+        }
+      }
+    }
+    if (ap.cluster) {
+      namespace cg = cooperative_groups;
+      cg::cluster_group cluster = cg::this_cluster();
+      const int S = ap.splits;                // the cluster's CTAs; this one is rank `split`
+      const int nblk = (g * D + kThreads - 1) / kThreads, jmax = (nblk + S - 1) / S;
+      // every CTA of the cluster is past its main loop
+      asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+      if (tid < g)
+        for (int r = 0; r < S; ++r) {
+          float* d = cluster.map_shared_rank(rml, r) + split * 16;
+          d[tid] = hM;
+          d[8 + tid] = hL;
+        }
+  #pragma unroll
+      for (int k = 0; k < kBlk; ++k)
+        if (k * kThreads + tid < g * D)
+          cluster.map_shared_rank(racc, k % S)[(split * jmax + k / S) * kThreads + tid] = Ab[k];
+      // the writes into every CTA are complete and visible to it
+      asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+      asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+      float* pm = wo;                         // [g][S] rescale weight of each split
+      if (tid < g) {
+        float M = -INFINITY, Ls = 0.0f;
+        for (int sp = 0; sp < S; ++sp) M = fmaxf(M, rml[sp * 16 + tid]);
+        for (int sp = 0; sp < S; ++sp) {
+          const float f = rescale(rml[sp * 16 + tid], M);
+          Ls += rml[sp * 16 + 8 + tid] * f;
+          pm[tid * S + sp] = f;
+        }
+        fin[tid] = M;
+        fin[8 + tid] = Ls;
+      }
+      __syncthreads();
+      // this split's share of the output: blocks split, split + S, ...
+      for (int j = 0; j < jmax; ++j) {
+        const int idx = (split + j * S) * kThreads + tid;
+        if (idx < g * D) {
+          const int h = idx / D, dd = idx - h * D;
+          float A = 0.0f;
+          for (int sp = 0; sp < S; ++sp) A += racc[(sp * jmax + j) * kThreads + tid] * pm[h * S + sp];
+          outp[h * D + dd] = A / fin[8 + h];
+        }
+      }
+    }
+  } else {
+    ss.lA = gsum8(ss.lA);
+    ss.lB = gsum8(ss.lB);
+    remove_offset();
+    __syncthreads();
+    float* cml = wo + kWarps * 8 * D;                      // cluster: this split's [2][8] max, sum
+    float* cacc = cml + 16;                                // cluster: this split's [8][D] output
+    const float unscale = pow2i(-ss.E);
+    if (gid == 0) {
+      wm[warp * 8 + 2 * t4] = ss.mA;
+      wm[warp * 8 + 2 * t4 + 1] = ss.mB;
+      wl[warp * 8 + 2 * t4] = ss.lA;
+      wl[warp * 8 + 2 * t4 + 1] = ss.lB;
+    }
+  #pragma unroll
+    for (int mt = 0; mt < G::KS; ++mt) {
+      const int d0 = gid * G::VPT + 2 * mt;
+      float* oa = wo + (warp * 8 + 2 * t4) * D;
+      float* ob = oa + D;
+      oa[d0] = O[mt][0] * unscale;
+      ob[d0] = O[mt][1] * unscale;
+      oa[d0 + 1] = O[mt][2] * unscale;
+      ob[d0 + 1] = O[mt][3] * unscale;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < g * D; idx += kThreads) {
+      const int h = idx / D, dd = idx - h * D;
+      float M = -INFINITY;
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 8 + h]);
+      float Ls = 0.0f, A = 0.0f;
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = rescale(wm[w * 8 + h], M);
+        Ls += wl[w * 8 + h] * f;
+        A += wo[(w * 8 + h) * D + dd] * f;
+      }
+      if (ap.splits == 1) {
+        outp[h * D + dd] = A / Ls;
+        if (dd == 0) { fin[h] = M; fin[8 + h] = Ls; }
+      } else if (ap.cluster) {
+        cacc[h * D + dd] = A;
+        if (dd == 0) { cml[h] = M; cml[8 + h] = Ls; }
+      } else {
+        const size_t pi = (obase + h) * ap.splits + split;
+        ap.part_acc[pi * D + dd] = A;
+        if (dd == 0) { ap.part_ml[pi * 2] = M; ap.part_ml[pi * 2 + 1] = Ls; }
+      }
+    }
+    if (ap.cluster) {
+      namespace cg = cooperative_groups;
+      cg::cluster_group cluster = cg::this_cluster();
+      const int S = ap.splits;                // the cluster's CTAs; this one is rank `split`
+      cluster.sync();                         // every split's partial is in its shared memory
+      float* pm = wo;                         // [g][S] max, then rescale weight
+      float* pl = wo + 8 * 64;                // [g][S] sum
+      for (int x = tid; x < g * S; x += kThreads) {
+        const int h = x / S, sp = x - h * S;
+        const float* r = cluster.map_shared_rank(cml, sp);
+        pm[x] = r[h];
+        pl[x] = r[8 + h];
+      }
+      __syncthreads();
+      if (tid < g) {
+        float M = -INFINITY, Ls = 0.0f;
+        for (int sp = 0; sp < S; ++sp) M = fmaxf(M, pm[tid * S + sp]);
+        for (int sp = 0; sp < S; ++sp) {
+          const float f = rescale(pm[tid * S + sp], M);
+          Ls += pl[tid * S + sp] * f;
+          pm[tid * S + sp] = f;
+        }
+        fin[tid] = M;
+        fin[8 + tid] = Ls;
+      }
+      __syncthreads();
+      // this split's share of the output: blocks of kThreads elements, dealt
+      // round-robin over the splits
+      for (int idx = split * kThreads + tid; idx < g * D; idx += S * kThreads) {
+        const int h = idx / D, dd = idx - h * D;
+        float A = 0.0f;
+        for (int sp = 0; sp < S; ++sp)
+          A += cluster.map_shared_rank(cacc, sp)[h * D + dd] * pm[h * S + sp];
+        outp[h * D + dd] = A / fin[8 + h];
+      }
+      cluster.sync();                         // no CTA leaves while its partial may be read
     }
   }
-  if (ap.cluster) {
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
-    const int S = ap.splits;                // the cluster's CTAs; this one is rank `split`
-    cluster.sync();                         // every split's partial is in its shared memory
-    float* pm = wo;                         // [g][S] max, then rescale weight
-    float* pl = wo + 8 * 64;                // [g][S] sum
-    for (int x = tid; x < g * S; x += kThreads) {
-      const int h = x / S, sp = x - h * S;
-      const float* r = cluster.map_shared_rank(cml, sp);
-      pm[x] = r[h];
-      pl[x] = r[8 + h];
-    }
-    __syncthreads();
-    if (tid < g) {
-      float M = -INFINITY, Ls = 0.0f;
-      for (int sp = 0; sp < S; ++sp) M = fmaxf(M, pm[tid * S + sp]);
-      for (int sp = 0; sp < S; ++sp) {
-        const float f = rescale(pm[tid * S + sp], M);
-        Ls += pl[tid * S + sp] * f;
-        pm[tid * S + sp] = f;
-      }
-      fin[tid] = M;
-      fin[8 + tid] = Ls;
-    }
-    __syncthreads();
-    // this split's share of the output: blocks of kThreads elements, dealt
-    // round-robin over the splits
-    for (int idx = split * kThreads + tid; idx < g * D; idx += S * kThreads) {
-      const int h = idx / D, dd = idx - h * D;
-      float A = 0.0f;
-      for (int sp = 0; sp < S; ++sp)
-        A += cluster.map_shared_rank(cacc, sp)[h * D + dd] * pm[h * S + sp];
-      outp[h * D + dd] = A / fin[8 + h];
-    }
-    cluster.sync();                         // no CTA leaves while its partial may be read
-  } else if (ap.splits > 1) {
+  if (!ap.cluster && ap.splits > 1) {
     __shared__ int s_last;
     __threadfence();
     __syncthreads();
