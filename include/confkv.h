@@ -29,7 +29,11 @@
  *     the caller, and only touched by work enqueued on `stream` during the
  *     call.  `stream` is a cudaStream_t (NULL = legacy default stream).
  *   - The context owns all cache memory; it is single-threaded: calls on one
- *     context must not run concurrently from several host threads.
+ *     context must not run concurrently from several host threads.  The GPU
+ *     work of successive calls on one context must be ordered: the same
+ *     stream, or streams ordered by events (a call's inputs may come from
+ *     the kernel right before it in its stream, even one that lets its
+ *     dependents start early through programmatic dependent launch).
  *   - Calls return CONFKV_OK (0) or a negative CONFKV_ERR_* code.  Argument
  *     errors are detected on the host before any work is enqueued; the
  *     message is available from confkv_last_error().  Errors the GPU detects
