@@ -983,8 +983,9 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   float* outp = ap.out + (static_cast<size_t>(lbu) * c.Hq + kvh * g) * D;
   if constexpr (PL) {
     // Cluster: this CTA's tiles are all consumed; once every CTA of the
-    // cluster has said so, they write into each other's stage memory.
-    if (ap.cluster) asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+    // cluster has said so, they write into each other's stage memory.  (No
+    // release needed: every read of the stages has returned its value.)
+    if (ap.cluster) asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
     ss.lA = gsum8(ss.lA);
     ss.lB = gsum8(ss.lB);
     remove_offset();
@@ -1015,38 +1016,47 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       ob[d0 + 1] = O[mt][3] * unscale;
     }
     __syncthreads();
-    // per head: the CTA's (max, sum) and each warp's rescale factor to that max
-    float hM = 0.0f, hL = 0.0f;                            // thread tid < g: head tid's
-    if (tid < g) {
+    // per head: the CTA's (max, sum) and each warp's rescale factor to that
+    // max, computed by lane h of every warp (lane h < g: head h) and handed
+    // to the lanes that need it by shuffles, so no further CTA barrier
+    float hM, hL, hf[kWarps];
+    {
+      const int h = lane < g ? lane : 0;
       float M = -INFINITY;
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 8 + tid]);
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 8 + h]);
       float Ls = 0.0f;
+  #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float f = rescale(wm[w * 8 + tid], M);
-        Ls += wl[w * 8 + tid] * f;
-        wf[w * 8 + tid] = f;
+        hf[w] = rescale(wm[w * 8 + h], M);
+        Ls += wl[w * 8 + h] * hf[w];
       }
       hM = M;
       hL = Ls;
+    }
+    if (tid < g) {
       if (ap.splits == 1) {
-        fin[tid] = M;
-        fin[8 + tid] = Ls;
+        fin[tid] = hM;
+        fin[8 + tid] = hL;
       } else if (!ap.cluster) {
         const size_t pi = (obase + tid) * ap.splits + split;
-        ap.part_ml[pi * 2] = M;
-        ap.part_ml[pi * 2 + 1] = Ls;
+        ap.part_ml[pi * 2] = hM;
+        ap.part_ml[pi * 2 + 1] = hL;
       }
     }
-    __syncthreads();
+    if (ap.splits == 1) __syncthreads();               // fin is read below
     float Ab[kBlk];                                        // this thread's element of each block
   #pragma unroll
     for (int k = 0; k < kBlk; ++k) {
       const int idx = k * kThreads + tid;
+      // the head of this element is the same for the whole warp
+      const int h = idx / D, dd = idx - h * D;
+      float f[kWarps];
+  #pragma unroll
+      for (int w = 0; w < kWarps; ++w) f[w] = __shfl_sync(0xffffffffu, hf[w], h & 31);
       Ab[k] = 0.0f;
       if (idx < g * D) {
-        const int h = idx / D, dd = idx - h * D;
         float A = 0.0f;
-        for (int w = 0; w < kWarps; ++w) A += wo[(w * 8 + h) * D + dd] * wf[w * 8 + h];
+        for (int w = 0; w < kWarps; ++w) A += wo[(w * 8 + h) * D + dd] * f[w];
         Ab[k] = A;
         if (ap.splits == 1) {
           outp[h * D + dd] = A / fin[8 + h];
