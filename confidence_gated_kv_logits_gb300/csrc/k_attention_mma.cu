@@ -989,31 +989,43 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     ss.lA = gsum8(ss.lA);
     ss.lB = gsum8(ss.lB);
     remove_offset();
-    __syncthreads();
-    float* wf = wo + kWarps * 8 * D;                       // [kWarps][8]
-    // cluster: what the splits write into this CTA -- every split's per-head
-    // (max, sum) [S][2][8], and every split's partial of the output blocks this
-    // CTA finishes [S][jmax][kThreads] (output block k = k-th kThreads elements
-    // of the [g][D] output, finished by split k % S as its block k / S)
-    float* rml = wf + kWarps * 8;
+    // Each warp's partial -- per head (max, sum) [2][8], then [8][D] -- goes
+    // into its own stage memory, free once its own loop is done, so no CTA
+    // barrier is needed before it is written.  The first 80 floats of every
+    // warp's stage memory are skipped (warp 0's hold fin).
+    constexpr int kRegion = kStages * STAGE / 4;          // floats per warp's stages
+    constexpr int kPart = 80;                             // partial offset in a region
+    float* const sb = reinterpret_cast<float*>(smem);
+    // cluster: what the splits write into this CTA, after warp 0's partial --
+    // every split's per-head (max, sum) [S][2][8], and every split's partial of
+    // the output blocks this CTA finishes [S][jmax][kThreads] (output block k
+    // = k-th kThreads elements of the [g][D] output, finished by split k % S
+    // as its block k / S)
+    float* rml = sb + kPart + 16 + 8 * D;
     float* racc = rml + kMaxClusterSplits * 16;
     constexpr int kBlk = 8 * D / kThreads;                 // output blocks at most
+    static_assert(kPart + 16 + 8 * D + kMaxClusterSplits * 16 +
+                      (kBlk + kMaxClusterSplits - 1) * kThreads <= kRegion,
+                  "merge buffers exceed warp 0's stage memory");
     const float unscale = pow2i(-ss.E);
-    if (gid == 0) {
-      wm[warp * 8 + 2 * t4] = ss.mA;
-      wm[warp * 8 + 2 * t4 + 1] = ss.mB;
-      wl[warp * 8 + 2 * t4] = ss.lA;
-      wl[warp * 8 + 2 * t4 + 1] = ss.lB;
-    }
+    {
+      float* pw = sb + warp * kRegion + kPart;
+      if (gid == 0) {
+        pw[2 * t4] = ss.mA;
+        pw[2 * t4 + 1] = ss.mB;
+        pw[8 + 2 * t4] = ss.lA;
+        pw[8 + 2 * t4 + 1] = ss.lB;
+      }
   #pragma unroll
-    for (int mt = 0; mt < G::KS; ++mt) {
-      const int d0 = gid * G::VPT + 2 * mt;
-      float* oa = wo + (warp * 8 + 2 * t4) * D;
-      float* ob = oa + D;
-      oa[d0] = O[mt][0] * unscale;
-      ob[d0] = O[mt][1] * unscale;
-      oa[d0 + 1] = O[mt][2] * unscale;
-      ob[d0 + 1] = O[mt][3] * unscale;
+      for (int mt = 0; mt < G::KS; ++mt) {
+        const int d0 = gid * G::VPT + 2 * mt;
+        float* oa = pw + 16 + (2 * t4) * D;
+        float* ob = oa + D;
+        oa[d0] = O[mt][0] * unscale;
+        ob[d0] = O[mt][1] * unscale;
+        oa[d0 + 1] = O[mt][2] * unscale;
+        ob[d0 + 1] = O[mt][3] * unscale;
+      }
     }
     __syncthreads();
     // per head: the CTA's (max, sum) and each warp's rescale factor to that
@@ -1023,12 +1035,12 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     {
       const int h = lane < g ? lane : 0;
       float M = -INFINITY;
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 8 + h]);
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sb[w * kRegion + kPart + h]);
       float Ls = 0.0f;
   #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        hf[w] = rescale(wm[w * 8 + h], M);
-        Ls += wl[w * 8 + h] * hf[w];
+        hf[w] = rescale(sb[w * kRegion + kPart + h], M);
+        Ls += sb[w * kRegion + kPart + 8 + h] * hf[w];
       }
       hM = M;
       hL = Ls;
@@ -1056,7 +1068,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       Ab[k] = 0.0f;
       if (idx < g * D) {
         float A = 0.0f;
-        for (int w = 0; w < kWarps; ++w) A += wo[(w * 8 + h) * D + dd] * f[w];
+        for (int w = 0; w < kWarps; ++w) A += sb[w * kRegion + kPart + 16 + h * D + dd] * f[w];
         Ab[k] = A;
         if (ap.splits == 1) {
           outp[h * D + dd] = A / fin[8 + h];
@@ -1085,27 +1097,41 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       // the writes into every CTA are complete and visible to it
       asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
       asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-      float* pm = wo;                         // [g][S] rescale weight of each split
-      if (tid < g) {
+      // per head, by lane h < g of every warp: the merged (max, sum) over the
+      // splits and each split's rescale weight, shuffled to the lanes below
+      float pf[kMaxClusterSplits], fL;
+      {
+        const int h = lane < g ? lane : 0;
         float M = -INFINITY, Ls = 0.0f;
-        for (int sp = 0; sp < S; ++sp) M = fmaxf(M, rml[sp * 16 + tid]);
-        for (int sp = 0; sp < S; ++sp) {
-          const float f = rescale(rml[sp * 16 + tid], M);
-          Ls += rml[sp * 16 + 8 + tid] * f;
-          pm[tid * S + sp] = f;
+        for (int sp = 0; sp < S; ++sp) M = fmaxf(M, rml[sp * 16 + h]);
+  #pragma unroll
+        for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
+          pf[sp] = 0.0f;
+          if (sp < S) {
+            pf[sp] = rescale(rml[sp * 16 + h], M);
+            Ls += rml[sp * 16 + 8 + h] * pf[sp];
+          }
         }
-        fin[tid] = M;
-        fin[8 + tid] = Ls;
+        fL = Ls;
+        if (tid < g) {
+          fin[tid] = M;
+          fin[8 + tid] = Ls;
+        }
       }
-      __syncthreads();
       // this split's share of the output: blocks split, split + S, ...
       for (int j = 0; j < jmax; ++j) {
         const int idx = (split + j * S) * kThreads + tid;
+        const int h = idx / D, dd = idx - h * D;       // the same head for the whole warp
+        float wsp[kMaxClusterSplits];
+  #pragma unroll
+        for (int sp = 0; sp < kMaxClusterSplits; ++sp) wsp[sp] = __shfl_sync(0xffffffffu, pf[sp], h & 31);
+        const float Lh = __shfl_sync(0xffffffffu, fL, h & 31);
         if (idx < g * D) {
-          const int h = idx / D, dd = idx - h * D;
           float A = 0.0f;
-          for (int sp = 0; sp < S; ++sp) A += racc[(sp * jmax + j) * kThreads + tid] * pm[h * S + sp];
-          outp[h * D + dd] = A / fin[8 + h];
+  #pragma unroll
+          for (int sp = 0; sp < kMaxClusterSplits; ++sp)
+            if (sp < S) A += racc[(sp * jmax + j) * kThreads + tid] * wsp[sp];
+          outp[h * D + dd] = A / Lh;
         }
       }
     }
