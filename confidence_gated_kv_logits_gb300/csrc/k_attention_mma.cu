@@ -54,9 +54,11 @@
 // mass of its own tokens.  Launches that store the arriving token (per-layer
 // steps, where the merge is on each layer's critical path) push instead:
 // each CTA signals the end of its main loop on the cluster barrier, merges
-// its warps, waits for the others' signal and writes its per-head (max, sum)
-// into every CTA and its partial of each output block into the CTA that
-// finishes that block; one more cluster barrier, and every read is local.
+// its warps (each warp's partial in its own stage memory), waits for the
+// others' signal and sends, by asynchronous stores counted in bytes on the
+// receiver's mbarrier, its per-head (max, sum) to every CTA and its partial
+// of each output block to the CTA that finishes that block; each CTA waits
+// only for the bytes addressed to it, and every read is local.
 // With more splits the partials go through global memory and the CTA taking
 // the last ticket finishes the unit.
 #include <cooperative_groups.h>
@@ -222,6 +224,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, unsigned parity,
     if ((i & 31u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
   return false;
+}
+// Address of this CTA's shared variable `local` (shared::cta window) in CTA
+// `rank` of the cluster (shared::cluster window).
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+// Asynchronous 4-byte store into a cluster CTA's shared memory; its bytes
+// complete on that CTA's mbarrier `rbar` (shared::cluster addresses).
+__device__ __forceinline__ void st_async_f32(uint32_t raddr, float v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];\n" ::"r"(raddr),
+               "r"(__float_as_uint(v)), "r"(rbar)
+               : "memory");
 }
 // L2 policy for the streamed K/V tiles: evict first, so that the scores and
 // masses this kernel writes and re-reads stay resident
@@ -446,6 +462,9 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   unsigned char* smem =
       TMA ? smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) : smem_raw;
   __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
+  // per-layer launches in a cluster: completes when every split's merge data
+  // for this CTA has arrived
+  __shared__ __align__(8) unsigned long long rbar;
   const int unit = ap.lb0 * c.Hkv + blockIdx.x, split = blockIdx.y;
   const int lb = unit / c.Hkv, kvh = unit - lb * c.Hkv, g = c.g;
   const int lbu = lb - ap.lb0;                // index into the caller's q / out
@@ -497,6 +516,11 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
   if constexpr (TMA) {
     if (lane == 0)
       for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
+  }
+  if constexpr (PL) {
+    if (tid == 0) mbar_init(smem_u32(&rbar), 1);
+  }
+  if constexpr (TMA || PL) {
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     __syncwarp();
   }
@@ -1078,25 +1102,36 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
       }
     }
     if (ap.cluster) {
-      namespace cg = cooperative_groups;
-      cg::cluster_group cluster = cg::this_cluster();
       const int S = ap.splits;                // the cluster's CTAs; this one is rank `split`
       const int nblk = (g * D + kThreads - 1) / kThreads, jmax = (nblk + S - 1) / S;
       // every CTA of the cluster is past its main loop
       asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+      // asynchronous stores into each receiving CTA, counted in bytes on its
+      // rbar: this CTA then waits only for what is addressed to it, and no
+      // CTA leaves before everything written into it has arrived
+      const uint32_t lbar = smem_u32(&rbar);
       if (tid < g)
         for (int r = 0; r < S; ++r) {
-          float* d = cluster.map_shared_rank(rml, r) + split * 16;
-          d[tid] = hM;
-          d[8 + tid] = hL;
+          const uint32_t d = cluster_addr(smem_u32(rml + split * 16 + tid), r), rb = cluster_addr(lbar, r);
+          st_async_f32(d, hM, rb);
+          st_async_f32(d + 32, hL, rb);                    // rml[split][8 + tid]
         }
   #pragma unroll
       for (int k = 0; k < kBlk; ++k)
         if (k * kThreads + tid < g * D)
-          cluster.map_shared_rank(racc, k % S)[(split * jmax + k / S) * kThreads + tid] = Ab[k];
-      // the writes into every CTA are complete and visible to it
-      asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-      asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+          st_async_f32(cluster_addr(smem_u32(racc + (split * jmax + k / S) * kThreads + tid), k % S), Ab[k],
+                       cluster_addr(lbar, k % S));
+      if (tid == 0) {
+        // from each of the S splits: 2g floats of (max, sum), and its
+        // partial of every output block this CTA finishes
+        unsigned bytes = 0;
+        for (int k = split; k < nblk; k += S) bytes += 4u * static_cast<unsigned>(min(kThreads, g * D - k * kThreads));
+        mbar_expect_tx(lbar, static_cast<unsigned>(S) * (bytes + 8u * static_cast<unsigned>(g)));
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(lbar, 0))) {
+        if (lane == 0) atomicOr(c.err, 4);
+        mbar_wait(lbar, 0);                            // one more bounded wait before leaving
+      }
       // per head, by lane h < g of every warp: the merged (max, sum) over the
       // splits and each split's rescale weight, shuffled to the lanes below
       float pf[kMaxClusterSplits], fL;
