@@ -1317,7 +1317,7 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
     // mass is deferred: the raw scores and each head's (max, sum) are kept
     // for the next step's first kernel (launch_mass_finalise)
     if (PL && ap.defer_mass) {
-      __syncthreads();
+      // (thread h < g wrote fin[h] and fin[8 + h] itself on every path here)
       if ((!ap.cluster || split == 0) && tid < g) {
         float* f = c.fin + (static_cast<size_t>(lb) * c.Hq + kvh * g + tid) * 2;
         f[0] = fin[tid];
