@@ -79,6 +79,20 @@ def test_mixed_per_layer_and_whole_steps(splits):
     parity.check(parity.run(w, splits=splits, per_layer=lambda s: (s // 4) % 2 == 0))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("g,splits", [(1, 2), (3, 4), (5, 6), (8, 7), (8, 8), (5, 3), (1, 8)])
+def test_per_layer_cluster_merge_shapes(d, g, splits):
+    # A per-layer launch merges the splits of a unit by sending each CTA of
+    # the cluster the bytes it needs -- every split's per-head (max, sum) and
+    # the partials of the output blocks it finishes -- and each CTA waits for
+    # exactly that many.  Every group size, head dim and split count must
+    # deliver them all (a short count would end the wait and flag the step),
+    # including splits left without any chunk and partial output blocks.
+    Hkv = 2
+    w = small(L=2, Hq=g * Hkv, Hkv=Hkv, d=d, prefill=90, steps=8, N_high=60, N_low=80, W=24)
+    parity.check(parity.run(w, splits=splits, per_layer=True))
+
+
 def test_per_layer_state_errors():
     import confidence_gated_kv_logits_gb300 as pkg
     w = small()
