@@ -389,60 +389,66 @@ __device__ __forceinline__ float mass_term(float acc, float s, float ml, float i
   return acc + ex2(fmaf(s, kL2E, -ml)) * il;
 }
 
-// Attention mass of the tokens [lo[r], hi[r]) of both regions (r = 0 INT8,
-// 1 FP16) of one unit, summed over its g query heads, from the raw scores SC
-// (g rows of `slots`) into MS.  Both regions start 16-byte aligned (cap8 % 32
-// == 0, slots % 16 == 0), so four consecutive tokens of a head are one
-// 128-bit load.  Score lines are dropped from L2 once read.  Called by all
-// kThreads threads of the CTA.
-__device__ __forceinline__ void mass_rows(const float* SC, float* MS, int slots, int cap8, int g,
-                                          const float (&ML)[8], const float (&iL)[8],
-                                          const int (&lo)[2], const int (&hi)[2]) {
-  const int tid = threadIdx.x;
-  for (int region = 0; region < 2; ++region) {
-    const int base = region ? cap8 : 0;
-    const int jlo = lo[region] >> 2, jhi = (hi[region] + 3) >> 2;   // float4 groups of 4 tokens
-    // two float4 rows of every head per thread in flight; j runs from a
-    // multiple of 8 so that the 8 groups of a 128-byte line sit in one warp
-    for (int j0 = (jlo & ~7) + tid; j0 < jhi; j0 += 2 * kThreads) {
-      float4 sv[2][8];
+// Attention mass of every token of both regions (INT8 tokens [0, n8), FP16
+// tokens [0, n16)) of one unit, summed over its G query heads, from the raw
+// scores SC (G rows of `slots`) into MS.  Both regions start 16-byte aligned
+// (cap8 % 32 == 0, slots % 16 == 0), so four consecutive tokens of a head
+// are one 128-bit load ("group").  The groups of both regions form one index
+// space, the FP16 region's starting at a multiple of 8, and each thread has
+// up to kU groups of loads in flight, so that a unit of up to kU * kThreads
+// groups is one round of loads.  Score lines are dropped from L2 once read:
+// the 8 groups of a 128-byte line are read by 8 lanes of one warp.  Called by
+// all kThreads threads of the CTA.
+template <int G>
+__device__ __forceinline__ void mass_rows(const float* SC, float* MS, int slots, int cap8,
+                                          const float (&ML)[8], const float (&iL)[8], int n8, int n16) {
+  constexpr int kU = 3;
+  const int g8 = (n8 + 3) >> 2, g16 = (n16 + 3) >> 2;
+  const int q1 = (g8 + 7) & ~7;                 // first index of the FP16 region's groups
+  const int nq = q1 + g16;
+  for (int q0 = threadIdx.x; q0 < nq; q0 += kU * kThreads) {
+    float4 sv[kU][G];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int j = j0 + u * kThreads;
+    for (int u = 0; u < kU; ++u) {
+      const int q = q0 + u * kThreads;
+      const bool r16 = q >= q1;
+      const int j = r16 ? q - q1 : q;
+      if (r16 ? j < g16 : j < g8) {
+        const float* row = SC + (r16 ? cap8 : 0);
 #pragma unroll
-        for (int h = 0; h < 8; ++h)
-          if (h < g && j >= jlo && j < jhi)
-            sv[u][h] = __ldcg(reinterpret_cast<const float4*>(SC + static_cast<size_t>(h) * slots + base) + j);
+        for (int h = 0; h < G; ++h)
+          sv[u][h] = __ldcg(reinterpret_cast<const float4*>(row + static_cast<size_t>(h) * slots) + j);
       }
+    }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int j = j0 + u * kThreads;
-        if (j < jlo || j >= jhi) continue;
-        float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int u = 0; u < kU; ++u) {
+      const int q = q0 + u * kThreads;
+      const bool r16 = q >= q1;
+      const int j = r16 ? q - q1 : q;
+      if (!(r16 ? j < g16 : j < g8)) continue;
+      const int base = r16 ? cap8 : 0, hi = r16 ? n16 : n8;
+      float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-        for (int h = 0; h < 8; ++h)
-          if (h < g) {
-            a.x = mass_term(a.x, sv[u][h].x, ML[h], iL[h]);
-            a.y = mass_term(a.y, sv[u][h].y, ML[h], iL[h]);
-            a.z = mass_term(a.z, sv[u][h].z, ML[h], iL[h]);
-            a.w = mass_term(a.w, sv[u][h].w, ML[h], iL[h]);
-          }
-        // The raw scores are dead once read here (the next step rewrites every
-        // live slot before reading it): drop whole 128-byte lines of them from
-        // L2 so they are never written back.  The 8 lanes reading one line are
-        // in this warp; lines shared with a neighbouring row are kept.
-        __syncwarp(__activemask());
-        if ((j & 7) == 0 && 4 * j + 32 <= hi[region]) {
+      for (int h = 0; h < G; ++h) {
+        a.x = mass_term(a.x, sv[u][h].x, ML[h], iL[h]);
+        a.y = mass_term(a.y, sv[u][h].y, ML[h], iL[h]);
+        a.z = mass_term(a.z, sv[u][h].z, ML[h], iL[h]);
+        a.w = mass_term(a.w, sv[u][h].w, ML[h], iL[h]);
+      }
+      // The raw scores are dead once read here (the next step rewrites every
+      // live slot before reading it): drop whole 128-byte lines of them from
+      // L2 so they are never written back.  The 8 lanes reading one line are
+      // in this warp; lines shared with a neighbouring row are kept.
+      __syncwarp(__activemask());
+      if ((j & 7) == 0 && 4 * j + 32 <= hi) {
 #pragma unroll
-          for (int h = 0; h < 8; ++h)
-            if (h < g) {
-              const float* line = SC + static_cast<size_t>(h) * slots + base + 4 * j;
-              if ((reinterpret_cast<uintptr_t>(line) & 127u) == 0) l2_discard_line(line);
-            }
+        for (int h = 0; h < G; ++h) {
+          const float* line = SC + static_cast<size_t>(h) * slots + base + 4 * j;
+          if ((reinterpret_cast<uintptr_t>(line) & 127u) == 0) l2_discard_line(line);
         }
-        // slots past the region end hold stale scores; their mass is never read
-        reinterpret_cast<float4*>(MS + base)[j] = a;
       }
+      // slots past the region end hold stale scores; their mass is never read
+      reinterpret_cast<float4*>(MS + base)[j] = a;
     }
   }
 }
@@ -1403,25 +1409,31 @@ k_attn_mma(Cache c, AttnParams ap, const __grid_constant__ TmaMaps tm) {
 // as the attention's epilogue over every cached token.  The CTA clears the
 // unit's flag once done: the score lines it drops from L2 must never be read
 // again, so a second finalisation of the same step must do nothing.
+template <int G>
 __global__ void __launch_bounds__(kThreads) k_mass_finalise(Cache c) {
   pdl_trigger();     // the next kernel waits for this grid before it reads anything
   pdl_wait();        // the attention launches that kept the scores are complete
-  const int unit = blockIdx.x, lb = unit / c.Hkv, kvh = unit - lb * c.Hkv, g = c.g;
-  if (!c.mass_pending[unit]) return;
+  const int unit = blockIdx.x, lb = unit / c.Hkv, kvh = unit - lb * c.Hkv;
+  // the unit's flag, region sizes and per-head (max, sum), loaded together
+  const int pending = c.mass_pending[unit];
   const int n8 = c.n8[lb], n16 = c.n16[lb];
+  float fm = 0.0f, fs = 1.0f;
+  if (threadIdx.x < G) {
+    const float* f = c.fin + (static_cast<size_t>(lb) * c.Hq + kvh * G + threadIdx.x) * 2;
+    fm = f[0];
+    fs = f[1];
+  }
+  if (!pending) return;
   __shared__ float fin[16];
-  if (threadIdx.x < g) {
-    const float* f = c.fin + (static_cast<size_t>(lb) * c.Hq + kvh * g + threadIdx.x) * 2;
-    fin[threadIdx.x] = f[0];
-    fin[8 + threadIdx.x] = f[1];
+  if (threadIdx.x < G) {
+    fin[threadIdx.x] = fm;
+    fin[8 + threadIdx.x] = fs;
   }
   __syncthreads();
   float ML[8], iL[8];
-  mass_coeffs(fin, g, ML, iL);
-  const int lo[2] = {0, 0}, hi[2] = {n8, n16};
-  mass_rows(c.scores + (static_cast<size_t>(lb) * c.Hq + kvh * g) * c.slots,
-            c.mass + (static_cast<size_t>(lb) * c.Hkv + kvh) * c.slots, c.slots, c.cap8, g, ML, iL,
-            lo, hi);
+  mass_coeffs(fin, G, ML, iL);
+  mass_rows<G>(c.scores + (static_cast<size_t>(lb) * c.Hq + kvh * G) * c.slots,
+               c.mass + (static_cast<size_t>(lb) * c.Hkv + kvh) * c.slots, c.slots, c.cap8, ML, iL, n8, n16);
   if (threadIdx.x == 0) c.mass_pending[unit] = 0;     // only this CTA reads the unit's flag
 }
 
@@ -1577,7 +1589,18 @@ cudaError_t launch_attention_mma(const Cache& c, const AttnParams& ap, cudaStrea
 
 cudaError_t launch_mass_finalise(const Cache& c, cudaStream_t s) {
   const int units = c.L * c.B * c.Hkv;
-  const cudaError_t e = launch_pdl(k_mass_finalise, dim3(units), dim3(kThreads), 0, s, c);
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (c.g) {
+    case 1: e = launch_pdl(k_mass_finalise<1>, dim3(units), dim3(kThreads), 0, s, c); break;
+    case 2: e = launch_pdl(k_mass_finalise<2>, dim3(units), dim3(kThreads), 0, s, c); break;
+    case 3: e = launch_pdl(k_mass_finalise<3>, dim3(units), dim3(kThreads), 0, s, c); break;
+    case 4: e = launch_pdl(k_mass_finalise<4>, dim3(units), dim3(kThreads), 0, s, c); break;
+    case 5: e = launch_pdl(k_mass_finalise<5>, dim3(units), dim3(kThreads), 0, s, c); break;
+    case 6: e = launch_pdl(k_mass_finalise<6>, dim3(units), dim3(kThreads), 0, s, c); break;
+    case 7: e = launch_pdl(k_mass_finalise<7>, dim3(units), dim3(kThreads), 0, s, c); break;
+    case 8: e = launch_pdl(k_mass_finalise<8>, dim3(units), dim3(kThreads), 0, s, c); break;
+    default: return cudaSuccess;    // larger groups run the CUDA-core attention, which never defers
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
