@@ -657,6 +657,27 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaStream_t cs = c->cp_stream, ks = c->k_stream;
+  // When `out` (and c and the budgets, if asked for) are page-locked host
+  // memory mapped into the device's address space (cudaHostAlloc /
+  // cudaMallocHost memory under unified addressing), the kernels write them
+  // directly while the step runs, so no copy trails the attention and the
+  // attention is one launch; otherwise they go through the device staging
+  // buffers and copies back.  The kept lists always go through staging:
+  // the selection writes them at its very end, and waiting for them to cross
+  // the host link would hold back the attention, which waits for that grid.
+  auto mapped = [](void* p) -> void* {
+    if (!p) return nullptr;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+  };
+  float* out_d = static_cast<float*>(mapped(out));
+  float* cf_d = static_cast<float*>(mapped(conf_out));
+  int32_t* bd_d = static_cast<int32_t*>(mapped(budget_out));
+  const bool direct = out_d && (!conf_out || cf_d) && (!budget_out || bd_d);
   // once copies are enqueued, no return may leave one in flight (the
   // caller's host buffers are only borrowed for the call)
   auto drain = [&](int code) {
@@ -665,8 +686,9 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     cudaStreamSynchronize(s);
     return code;
   };
-  size_t cuts[kHostGroups + 1];
-  const int G = host_ranges(c, cuts);
+  size_t cuts[kHostGroups + 1] = {0, LB};
+  // direct outputs leave nothing to overlap with a second range
+  const int G = direct ? 1 : host_ranges(c, cuts);
   cudaEvent_t ev_start = c->cp_ev[0], ev_sel = c->cp_ev[1], ev_ready = c->cp_ev[2];
   const cudaEvent_t* ev_in = c->cp_ev + 3;
   const cudaEvent_t* ev_out = c->cp_ev + 3 + kHostGroups;
@@ -691,8 +713,8 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     if (rc != CONFKV_OK) return drain(rc);
   }
   if (uses_confidence(c)) {
-    rc = run_confidence(c, c->st_logits, conf_out ? c->st_conf : nullptr,
-                        budget_out ? c->st_bud : nullptr, s);
+    rc = run_confidence(c, c->st_logits, conf_out ? (direct ? cf_d : c->st_conf) : nullptr,
+                        budget_out ? (direct ? bd_d : c->st_bud) : nullptr, s);
     if (rc != CONFKV_OK) return drain(rc);
   }
   // the selection of every (layer, sequence), reserving the new tokens'
@@ -709,9 +731,9 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     A(cudaMemcpyAsync(kept_pos, c->st_kp, nkp * sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
   if (kept_count)
     A(cudaMemcpyAsync(kept_count, c->st_kc, LB * sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
-  if (conf_out && uses_confidence(c))
+  if (!direct && conf_out && uses_confidence(c))
     A(cudaMemcpyAsync(conf_out, c->st_conf, c->B * sizeof(float), cudaMemcpyDeviceToHost, cs));
-  if (budget_out && uses_confidence(c))
+  if (!direct && budget_out && uses_confidence(c))
     A(cudaMemcpyAsync(budget_out, c->st_bud, c->B * sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
   const bool fused = confkv::attention_uses_mma(c->cache, c->attn_kernel);
   if (!fused) {
@@ -736,15 +758,17 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
     const StepParams f = step_params(c, static_cast<int>(lb0), static_cast<int>(nlb),
                                      c->st_k + lb0 * c->Hkv * c->d, c->st_v + lb0 * c->Hkv * c->d,
                                      nullptr, nullptr);
-    rc = run_attention_timed(c, c->st_q + lb0 * c->Hq * c->d, c->st_out + lb0 * c->Hq * c->d, as,
-                             static_cast<int>(lb0), static_cast<int>(nlb), c->splits,
-                             fused ? &f : nullptr);
+    float* dst = (direct ? out_d : c->st_out) + lb0 * c->Hq * c->d;
+    rc = run_attention_timed(c, c->st_q + lb0 * c->Hq * c->d, dst, as, static_cast<int>(lb0),
+                             static_cast<int>(nlb), c->splits, fused ? &f : nullptr);
     if (rc != CONFKV_OK) return drain(rc);
-    A(cudaEventRecord(ev_out[gi], as));
-    A(cudaStreamWaitEvent(cs, ev_out[gi], 0));
-    const size_t oq = lb0 * c->Hq * c->d;
-    A(cudaMemcpyAsync(out + oq, c->st_out + oq, nlb * c->Hq * c->d * sizeof(float),
-                      cudaMemcpyDeviceToHost, cs));
+    if (!direct) {
+      A(cudaEventRecord(ev_out[gi], as));
+      A(cudaStreamWaitEvent(cs, ev_out[gi], 0));
+      const size_t oq = lb0 * c->Hq * c->d;
+      A(cudaMemcpyAsync(out + oq, c->st_out + oq, nlb * c->Hq * c->d * sizeof(float),
+                        cudaMemcpyDeviceToHost, cs));
+    }
   }
   if (G > 1) A(cudaStreamWaitEvent(s, ev_out[G - 1], 0));     // `stream` covers every range
   c->t += 1;

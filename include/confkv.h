@@ -262,14 +262,20 @@ int confkv_step_layer(confkv_ctx* ctx, int layer, const uint16_t* q, const uint1
 /*
  * confkv_step_host -- confkv_step with HOST buffers of the same layouts.
  * Copies the inputs to context-owned device staging buffers, runs the step
- * and copies the outputs back, then waits for both.  The copies overlap the
+ * and returns the outputs, then waits for all of it.  The copies overlap the
  * compute: logits go first on `stream`; q, k_new and v_new travel on a
  * context-owned copy stream while the confidence and the selection (which do
- * not read them) run; large steps run the attention as two launches over
- * consecutive (layer, sequence) ranges (the second on a second context-owned
- * stream, so the grids overlap), the first range's outputs copied back while
- * the second computes.  Pinned host memory makes the copies
- * asynchronous DMA; pageable memory works but is slower.  NULL optional
+ * not read them) run; the kept lists go back during the attention.  When
+ * `out` (and conf_out and budget_out, if given) is page-locked host memory
+ * mapped into the device's address space (cudaHostAlloc / cudaMallocHost
+ * memory under unified addressing), the kernels write those outputs into it
+ * directly as they produce them, and the attention is one launch.
+ * Otherwise those outputs go through staging too: large steps then run the
+ * attention as two launches over consecutive (layer, sequence) ranges (the
+ * second on a second context-owned stream, so the grids overlap), the first
+ * range's outputs copied back while the second computes.  Pinned host
+ * memory makes the copies asynchronous DMA; pageable memory works but is
+ * slower.  NULL optional
  * outputs are skipped.  The results equal confkv_step's bit for bit, except
  * that kept_pos entries past kept_count are unspecified here (the whole
  * staging row is copied back).  The call synchronises, so it cannot be

@@ -30,14 +30,23 @@ def _pinned(shape, dtype):
     return torch.zeros(shape, dtype=dtype).pin_memory().numpy()
 
 
+def _pageable(shape, dtype):
+    return torch.zeros(shape, dtype=dtype).numpy()
+
+
 @pytest.mark.parametrize("shape", [
     dict(L=3, B=2, Hq=8, Hkv=2, d=128, V=500, prefill=60, steps=12, N_high=40, N_low=56, P=6, W=20),
     dict(L=2, B=3, Hq=16, Hkv=2, d=64, V=300, prefill=30, steps=10, N_high=24, N_low=40, P=4, W=12),
-    # 4096 units at d = 128: the attention runs as two ranges with overlapped copies
+    # 4096 units at d = 128: with pageable outputs the attention runs as two
+    # ranges with overlapped copies; pinned outputs are written directly
     dict(L=32, B=16, Hq=16, Hkv=8, d=128, V=64, prefill=40, steps=5, N_high=24, N_low=36, P=4, W=12),
 ])
 @pytest.mark.parametrize("kernel", [0, 1])
-def test_step_host_equals_device_step(shape, kernel):
+@pytest.mark.parametrize("outs", ["pinned", "pageable"])
+def test_step_host_equals_device_step(shape, kernel, outs):
+    # pinned (mapped) outputs are written by the kernels directly; pageable
+    # ones go through device staging buffers and copies
+    alloc = _pinned if outs == "pinned" else _pageable
     w = wl.Workload(name="host", **shape)
     a = _prefilled(w, attn_kernel=kernel)
     b = _prefilled(w, attn_kernel=kernel)
@@ -55,12 +64,12 @@ def test_step_host_equals_device_step(shape, kernel):
             h = _pinned(x.shape, torch.float32 if x.dtype == np.float32 else torch.float16)
             h[...] = x
             hin.append(h)
-        ob = _pinned((w.L, w.B, w.Hq, w.d), torch.float32)
-        kpb = _pinned((w.L, w.B, b.Ncap), torch.int32)
+        ob = alloc((w.L, w.B, w.Hq, w.d), torch.float32)
+        kpb = alloc((w.L, w.B, b.Ncap), torch.int32)
         kpb[...] = -1
-        kcb = _pinned((w.L, w.B), torch.int32)
-        cfb = _pinned((w.B,), torch.float32)
-        bdb = _pinned((w.B,), torch.int32)
+        kcb = alloc((w.L, w.B), torch.int32)
+        cfb = alloc((w.B,), torch.float32)
+        bdb = alloc((w.B,), torch.int32)
         b.step_host(*hin, ob, kpb, kcb, cfb, bdb)
         assert np.array_equal(ob.view(np.uint32), oa.cpu().numpy().view(np.uint32))
         assert np.array_equal(kcb, kca.cpu().numpy())
