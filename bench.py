@@ -649,9 +649,11 @@ def run_ours(args):
         d2h = h_out.nbytes + h_kp.nbytes + h_kc.nbytes + h_cf.nbytes + h_bd.nbytes
         e2e = {"value": ws * w.B * Ke / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": Ke,
-               "note": "confkv_step_host: pinned host inputs copied in, outputs (attention "
-                       "output, kept lists, c, budgets) copied out, every step; each pinned "
-                       "input set was read once by DMA before the timed region"}
+               "note": "confkv_step_host: pinned host inputs copied in every step; of the "
+                       "outputs, the attention output, c and the budgets are written by the "
+                       "kernels straight into the mapped pinned buffers and the kept lists "
+                       "are copied out; each pinned input set was read once by DMA before "
+                       "the timed region"}
         kv.close()
         del host_in
 
