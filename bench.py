@@ -18,8 +18,8 @@ so no flush is needed between steps.
 The JSON line carries the device-timed value, the attention's roofline
 (algorithmic bytes over its CUDA-event time, against the measured copy peak,
 with the DRAM traffic of the committed ncu capture), `e2e` (the same metric
-through confkv_step_host with pinned host buffers, copies inside the timed
-region), the CPU oracle baseline, the full-KV and sliding-window baselines on
+through confkv_step_host with pinned host buffers, every step's transfers
+inside the timed region), the CPU oracle baseline, the full-KV and sliding-window baselines on
 the same kernels, SM clocks sampled during the timed region and the number
 of kernel launches.  --per-layer and --graph time a captured step replayed
 as every step (per-layer entry points, or one whole step).
