@@ -463,6 +463,8 @@ StepParams step_params(const confkv_ctx* c, int lb0, int nlb, const uint16_t* k_
 // The masses that per-layer attention launches deferred, computed before
 // anything reads them (a no-op on the device for lanes with nothing pending).
 int run_mass_finalise(confkv_ctx* c, cudaStream_t s) {
+  // only the tensor-core attention defers the mass (per-layer launches)
+  if (!confkv::attention_uses_mma(c->cache, c->attn_kernel)) return CONFKV_OK;
   const cudaError_t e = confkv::launch_mass_finalise(c->cache, s);
   if (e != cudaSuccess) return fail(c, CONFKV_ERR_CUDA, std::string("mass finalise: ") + cudaGetErrorString(e));
   c->launches += 1;
