@@ -668,7 +668,8 @@ int confkv_step_host(confkv_ctx* c, const float* logits, const uint16_t* q,
   // the selection writes them at its very end, and waiting for them to cross
   // the host link would hold back the attention, which waits for that grid.
   auto mapped = [](void* p) -> void* {
-    if (!p) return nullptr;
+    // (the kernels store 4-byte words: a misaligned buffer goes through staging)
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 3u)) return nullptr;
     cudaPointerAttributes at{};
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
       (void)cudaGetLastError();

@@ -129,3 +129,26 @@ def test_step_host_policies(policy):
         assert np.array_equal(kcb, kca.cpu().numpy())
     a.close()
     b.close()
+
+
+def test_step_host_misaligned_pinned_output():
+    # A pinned output that is not 4-byte aligned cannot take the kernels'
+    # direct 4-byte stores: the call must route it through staging (checked
+    # on the host before anything is enqueued) and return the same bits.
+    w = wl.Workload(name="host", L=2, B=2, Hq=8, Hkv=2, d=128, V=300, prefill=30, steps=4,
+                    N_high=24, N_low=32, P=4, W=12)
+    a = _prefilled(w)
+    b = _prefilled(w)
+    n = w.L * w.B * w.Hq * w.d
+    raw = torch.zeros(4 * n + 8, dtype=torch.uint8).pin_memory().numpy()
+    ob = np.frombuffer(raw, dtype=np.float32, count=n, offset=2).reshape(w.L, w.B, w.Hq, w.d)
+    assert ob.ctypes.data % 4 == 2 and ob.flags.c_contiguous
+    for s in range(w.steps):
+        lg, q, k, v = (np.ascontiguousarray(x) for x in wl.step_inputs(w, s))
+        oa = torch.zeros(w.L, w.B, w.Hq, w.d, device=DEV)
+        a.step(*[torch.from_numpy(x).to(DEV) for x in (lg, q, k, v)], oa)
+        b.step_host(lg, q, k, v, ob)
+        assert np.array_equal(ob.view(np.uint32), oa.cpu().numpy().view(np.uint32))
+    assert a.stats()[1] == b.stats()[1] == 0
+    a.close()
+    b.close()
