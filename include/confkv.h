@@ -266,10 +266,11 @@ int confkv_step_layer(confkv_ctx* ctx, int layer, const uint16_t* q, const uint1
  * compute: logits go first on `stream`; q, k_new and v_new travel on a
  * context-owned copy stream while the confidence and the selection (which do
  * not read them) run; the kept lists go back during the attention.  When
- * `out` (and conf_out and budget_out, if given) is page-locked host memory
- * mapped into the device's address space (cudaHostAlloc / cudaMallocHost
- * memory under unified addressing), the kernels write those outputs into it
- * directly as they produce them, and the attention is one launch.
+ * `out` (and conf_out and budget_out, if given) is 4-byte-aligned
+ * page-locked host memory mapped into the device's address space
+ * (cudaHostAlloc / cudaMallocHost memory under unified addressing), the
+ * kernels write those outputs into it directly as they produce them, and
+ * the attention is one launch.
  * Otherwise those outputs go through staging too: large steps then run the
  * attention as two launches over consecutive (layer, sequence) ranges (the
  * second on a second context-owned stream, so the grids overlap), the first
